@@ -1,0 +1,361 @@
+"""Benchmark of the continuous softmax attention forward pass on GB300.
+
+One step = one csa_forward call (the whole hot path: TMA staging, QK^T on
+tensor cores, halo + correction b + online softmax, PV on tensor cores,
+epilogue) over the headline workload B=1, H=32, T=8192, d=128, bf16,
+scale 1/sqrt(d), zero sink, with inputs resident in HBM.  L2 is flushed
+(a 512 MiB write) before every timed step; each step is timed with CUDA
+events on the launching stream and the steps are summed.
+
+Also reported on the same JSON line:
+  e2e          the same metric through the C ABI with host buffers: pinned
+               host -> device copies of q, k, v, the kernel, and the
+               device -> host copy of o and lse, all inside the timed region
+  std          the library's standard causal attention kernel (eq. (12)) at
+               the same shape, and the ratio continuous / standard
+  roofline     tensor-core bound: algorithmic matmul flops / kernel time
+               against the measured dense bf16 peak
+  cpu_baseline the CPU oracle (double precision, all host cores) on a
+               bounded sample of rows of the same workload
+  clocks       nvidia-smi SM clocks and throttle reasons sampled during the
+               timed region
+
+`--impl reference` times the CPU oracle alone (the reference arm).
+Multi-GPU (torchrun): every rank runs its own copy of the workload (the
+(b, h) problems are independent; no collective on the data path), the time
+is the max over ranks, and value = all ranks' flops / that time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "continuous-attn fwd TFLOP/s (B=1,H=32,T=8192,d=128, bf16, causal)"
+UNIT = "TFLOP/s"
+WORKLOAD = "headline"
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (every 100 ms)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.tmp is None:
+            return None
+        try:
+            rows = [l.strip().split(", ") for l in open(self.tmp.name) if l.strip()]
+            os.unlink(self.tmp.name)
+        except Exception:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        load = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import continuous_softmax_attention_gb300 as csa
+    from continuous_softmax_attention_gb300.inputs import WORKLOADS, algorithmic_flops, workload_inputs
+
+    ws, rank, local = _dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[WORKLOAD]
+    B, H, T, d = w.B, w.H, w.T, w.d
+    scale = 1.0 / math.sqrt(d)
+    x = workload_inputs(WORKLOAD)
+    g = {k: v.to(dev) for k, v in x.items()}
+    out = torch.empty_like(g["q"])
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    flops = algorithmic_flops(B, H, T, d, continuous=True)
+    flops_std = algorithmic_flops(B, H, T, d, continuous=False)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def timed(fn, steps):
+        ms = []
+        for _ in range(steps):
+            flush.fill_(1.0)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return ms
+
+    csa_call = lambda: csa.forward(g["q"], g["k"], g["v"], mode=w.modes[0], scale=scale, out=out, lse=lse)
+    std_call = lambda: csa.std_forward(g["q"], g["k"], g["v"], scale=scale, out=out, lse=lse)
+
+    # end to end through the C ABI with host buffers
+    pin = {k: x[k].pin_memory() for k in ("q", "k", "v")}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq, dk, dv = (torch.empty_like(g[n]) for n in ("q", "k", "v"))
+
+    def e2e_call():
+        dq.copy_(pin["q"], non_blocking=True)
+        dk.copy_(pin["k"], non_blocking=True)
+        dv.copy_(pin["v"], non_blocking=True)
+        csa.forward(dq, dk, dv, mode=w.modes[0], scale=scale, out=out, lse=lse)
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+
+    h2d = sum(pin[n].numel() * pin[n].element_size() for n in pin)
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+
+    for _ in range(args.warmup):
+        csa_call()
+        std_call()
+        e2e_call()
+    torch.cuda.synchronize()
+    assert csa.device_status() == 0
+
+    barrier()
+    t_wall = time.perf_counter()
+    with ClockSampler(local) as clk:
+        ms_csa = timed(csa_call, args.steps)
+        ms_std = timed(std_call, args.steps)
+        ms_e2e = timed(e2e_call, args.steps)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    status = csa.device_status()
+
+    def total(ms):
+        t = torch.tensor([sum(ms)], dtype=torch.float64, device=dev)
+        if ws > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return t.item()
+
+    tot_csa, tot_std, tot_e2e = total(ms_csa), total(ms_std), total(ms_e2e)
+    if ws > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+    K = args.steps
+    ms_step = tot_csa / K
+    value = ws * flops * K / (tot_csa * 1e-3) / 1e12
+    std_value = ws * flops_std * K / (tot_std * 1e-3) / 1e12
+    e2e_value = ws * flops * K / (tot_e2e * 1e-3) / 1e12
+    burst, sustained, src = _peaks()
+    clocks = clk.summary()
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "T": T, "d": d, "scale": scale,
+                   "k0_mode": "zero", "causal": True, "per_gpu": "full workload per rank",
+                   "l2": "flushed (512 MiB write) before every timed step; inputs 192 MiB > L2"},
+        "tokens_per_s": round(ws * B * T * K / (tot_csa * 1e-3), 1),
+        "pct_bf16_peak": round(100.0 * achieved / burst, 2),
+        "std": {"value": round(std_value, 3), "unit": UNIT, "ms_per_step": round(tot_std / K, 5),
+                "ratio_continuous_over_std": round(value / std_value, 4)},
+        "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "ms_per_step": round(tot_e2e / K, 5),
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": K,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": burst,
+                     "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
+                     "peak_source": f"{src} bf16 dense (burst)", "traffic": None},
+        "clocks": clocks,
+        "device_status": status,
+        "wall_s": round(t_wall, 3),
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = cpu_baseline(x, scale, budget_s=args.cpu_seconds)
+    return line
+
+
+def _sample_rows(T, H, nrows, seed=0):
+    import numpy as np
+
+    rng = np.random.default_rng(seed)
+    picks = [(0, int(h), int(r)) for h, r in zip(rng.integers(0, H, nrows), rng.integers(0, T, nrows))]
+    return picks
+
+
+def cpu_baseline(x, scale, budget_s=15.0, seed=0):
+    """The oracle (eq. (8), double, all host cores) on rows sampled uniformly
+    from the workload; rate = algorithmic flops of those rows / wall time."""
+    import numpy as np
+
+    import oracle
+
+    B, H, T, d = x["q"].shape
+    q = x["q"].float().numpy()
+    k = x["k"].float().numpy()
+    v = x["v"].float().numpy()
+    cores = oracle.default_threads()
+    # calibrate on a small sample, then size the timed one to the budget
+    n = 16 * cores
+    while True:
+        picks = _sample_rows(T, H, n, seed)
+        rows = oracle.flat_rows(B, H, T, picks)
+        t0 = time.perf_counter()
+        oracle.forward_rows(q, k, v, rows, scale=scale, nthreads=cores)
+        dt = time.perf_counter() - t0
+        if dt > 0.25 * budget_s or n >= 1 << 20:
+            break
+        n = int(n * min(8.0, max(2.0, 0.5 * budget_s / max(dt, 1e-3))))
+    pairs = sum(r + 2 for (_, _, r) in picks)
+    rate = 4.0 * d * pairs / dt / 1e12
+    return {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(picks)} rows drawn uniformly from the {B}x{H}x{T}x{d} workload "
+                      f"(eq. (8) in double, {dt:.1f} s)",
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle on bounded samples of the same workload."""
+    import numpy as np
+
+    from continuous_softmax_attention_gb300.inputs import WORKLOADS, workload_inputs
+
+    import oracle
+
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return None
+    w = WORKLOADS[WORKLOAD]
+    x = workload_inputs(WORKLOAD)
+    q, k, v = (x[n].float().numpy() for n in ("q", "k", "v"))
+    B, H, T, d = q.shape
+    scale = 1.0 / math.sqrt(d)
+    cores = oracle.default_threads()
+    rows_per_step = max(cores, int(args.ref_rows))
+    for s in range(args.warmup):
+        picks = _sample_rows(T, H, max(cores, rows_per_step // 8), seed=100 + s)
+        oracle.forward_rows(q, k, v, oracle.flat_rows(B, H, T, picks), scale=scale, nthreads=cores)
+    tot = 0.0
+    flops = 0.0
+    for s in range(args.steps):
+        picks = _sample_rows(T, H, rows_per_step, seed=s)
+        rows = oracle.flat_rows(B, H, T, picks)
+        t0 = time.perf_counter()
+        oracle.forward_rows(q, k, v, rows, scale=scale, nthreads=cores)
+        tot += time.perf_counter() - t0
+        flops += 4.0 * d * sum(r + 2 for (_, _, r) in picks)
+    value = flops / tot / 1e12
+    sample = (f"{rows_per_step} rows per step drawn uniformly from the {B}x{H}x{T}x{d} workload "
+              f"(eq. (8) in double on {cores} host threads)")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "T": T, "d": d, "scale": scale,
+                   "k0_mode": "zero", "causal": True},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=256, help="oracle rows per reference step")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

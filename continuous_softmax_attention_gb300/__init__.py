@@ -6,5 +6,18 @@ binding over that library; nothing here computes attention.  Calls fail
 loudly when the library has not been built.
 """
 from .inputs import ZERO, COPY_FIRST, GIVEN  # noqa: F401
+from ._lib import (  # noqa: F401
+    CsaError,
+    device_status,
+    forward,
+    logphi2_eval,
+    segment_weights_eval,
+    selftest_wait_timeout,
+    status_string,
+    std_forward,
+)
 
-__all__ = ["ZERO", "COPY_FIRST", "GIVEN"]
+__all__ = [
+    "ZERO", "COPY_FIRST", "GIVEN", "CsaError", "forward", "std_forward", "logphi2_eval",
+    "segment_weights_eval", "device_status", "selftest_wait_timeout", "status_string",
+]

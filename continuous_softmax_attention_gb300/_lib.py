@@ -1,0 +1,212 @@
+"""ctypes binding of libcsa.so (C ABI declared in include/csa.h).
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, their data pointers and torch's current stream are passed to the
+C entry point, and a non-zero status becomes a CsaError.  Every step of the
+computation runs in the library's CUDA kernels; there is no other path.  If
+the library has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libcsa.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "csa.h")
+
+CSA_OK = 0
+CSA_ERR_INVALID_ARG = -1
+CSA_ERR_UNSUPPORTED = -2
+CSA_ERR_ALIGNMENT = -3
+CSA_ERR_CUDA = -4
+CSA_ERR_TIMEOUT = -5
+CSA_ERR_NO_DEVICE = -6
+
+
+class CsaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+_lib = None
+
+
+def load():
+    """Loads libcsa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -m continuous_softmax_attention_gb300.build` (no other compute path exists)")
+    lib = ctypes.CDLL(LIB_PATH)
+    p, i, f, u = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint
+    fwd = [p, p, p, p, p, p, p, i, i, i, i, f, i, p]
+    std = [p, p, p, p, p, i, i, i, i, f, p]
+    for name, args in (("csa_forward", fwd), ("csa_forward_f32", fwd),
+                       ("csa_std_forward", std), ("csa_std_forward_f32", std),
+                       ("csa_logphi2_eval", [p, p, i, p]),
+                       ("csa_segment_weights_eval", [p, p, p, p, i, p]),
+                       ("csa_device_status", []),
+                       ("csa_selftest_wait_timeout", [u, p]),
+                       ("csa_abi_version", [])):
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = i
+    lib.csa_status_string.argtypes = [i]
+    lib.csa_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().csa_status_string(int(code)).decode()
+    except Exception:  # library missing: fall back to the number
+        return f"status {code}"
+
+
+def header_functions(path: str = HEADER):
+    """Names of the functions declared in include/csa.h."""
+    src = open(path).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(csa_[a-z0-9_]+)\s*\(", src)))
+
+
+def _check(code: int, where: str):
+    if code != CSA_OK:
+        raise CsaError(code, where)
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_tensor(t, name, dtype, shape, device):
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def forward(q, k, v, k0=None, v0=None, *, mode: int = 0, scale=None, out=None, lse=None,
+            stream=None, want_lse: bool = True):
+    """Causal continuous softmax attention.  Returns (o, lse).
+
+    q, k, v: CUDA tensors [B, H, T, d], all bf16 (tensor-core kernel for
+    d in {64, 128}) or all fp32 (CUDA-core kernel).  k0, v0: [H, d], read
+    in mode GIVEN (2).  mode: 0 zero sink, 1 copy of the first token,
+    2 given.  scale defaults to 1/sqrt(d)."""
+    import torch
+
+    B, H, T, d = q.shape
+    dtype, dev = q.dtype, q.device
+    for name, t in (("k", k), ("v", v)):
+        _check_tensor(t, name, dtype, (B, H, T, d), dev)
+    _check_tensor(q, "q", dtype, (B, H, T, d), dev)
+    if mode == 2:
+        if k0 is None or v0 is None:
+            raise ValueError("mode 2 (given sink) needs k0 and v0")
+        _check_tensor(k0, "k0", dtype, (H, d), dev)
+        _check_tensor(v0, "v0", dtype, (H, d), dev)
+    else:
+        k0 = v0 = None
+    if scale is None:
+        scale = 1.0 / d ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    _check_tensor(out, "out", dtype, (B, H, T, d), dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _check_tensor(lse, "lse", torch.float32, (B, H, T), dev)
+    lib = load()
+    if dtype == torch.bfloat16:
+        fn, where = lib.csa_forward, "csa_forward"
+    elif dtype == torch.float32:
+        fn, where = lib.csa_forward_f32, "csa_forward_f32"
+    else:
+        raise ValueError(f"unsupported dtype {dtype}")
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(k0), _ptr(v0), _ptr(out), _ptr(lse),
+              B, H, T, d, float(scale), int(mode), _stream_handle(stream)), where)
+    return out, lse
+
+
+def std_forward(q, k, v, *, scale=None, out=None, lse=None, stream=None, want_lse: bool = True):
+    """Standard causal softmax attention (b = 0, no sink).  Returns (o, lse)."""
+    import torch
+
+    B, H, T, d = q.shape
+    dtype, dev = q.dtype, q.device
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(t, name, dtype, (B, H, T, d), dev)
+    if scale is None:
+        scale = 1.0 / d ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    _check_tensor(out, "out", dtype, (B, H, T, d), dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _check_tensor(lse, "lse", torch.float32, (B, H, T), dev)
+    lib = load()
+    if dtype == torch.bfloat16:
+        fn, where = lib.csa_std_forward, "csa_std_forward"
+    elif dtype == torch.float32:
+        fn, where = lib.csa_std_forward_f32, "csa_std_forward_f32"
+    else:
+        raise ValueError(f"unsupported dtype {dtype}")
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, T, d, float(scale),
+              _stream_handle(stream)), where)
+    return out, lse
+
+
+def logphi2_eval(x, stream=None):
+    """log phi2 of a float32 CUDA tensor, by the library's device function."""
+    import torch
+
+    x = x.contiguous()
+    if x.dtype != torch.float32 or not x.is_cuda:
+        raise ValueError("x must be a float32 CUDA tensor")
+    y = torch.empty_like(x)
+    _check(load().csa_logphi2_eval(_ptr(x), _ptr(y), x.numel(), _stream_handle(stream)),
+           "csa_logphi2_eval")
+    return y
+
+
+def segment_weights_eval(u0, u1, stream=None):
+    """(right, left) end weights of intervals (u0 -> u1), tensor-core kernel math."""
+    import torch
+
+    u0, u1 = u0.contiguous(), u1.contiguous()
+    r = torch.empty_like(u0)
+    l_ = torch.empty_like(u0)
+    _check(load().csa_segment_weights_eval(_ptr(u0), _ptr(u1), _ptr(r), _ptr(l_), u0.numel(),
+                                           _stream_handle(stream)), "csa_segment_weights_eval")
+    return r, l_
+
+
+def device_status() -> int:
+    """Reads and clears the library's device status word (synchronises)."""
+    return int(load().csa_device_status())
+
+
+def selftest_wait_timeout(timeout_us: int, stream=None):
+    _check(load().csa_selftest_wait_timeout(int(timeout_us), _stream_handle(stream)),
+           "csa_selftest_wait_timeout")

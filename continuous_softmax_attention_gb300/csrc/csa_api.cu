@@ -1,0 +1,163 @@
+// C ABI of libcsa.so (declared in include/csa.h): argument validation and
+// dispatch to the CUDA-core and tensor-core kernels.  No allocation, no
+// host synchronisation on the compute entry points.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "csa.h"
+#include "csa_internal.h"
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Common checks of the attention entry points.  Returns CSA_OK, or the
+// error code; *empty is set when there is nothing to compute.
+int check_common(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+                 const void *out, int B, int H, int T, int d, float scale, int mode, bool use_sink,
+                 bool *empty) {
+    *empty = false;
+    if (B < 0 || H < 0 || T < 0 || d < 1) return CSA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return CSA_ERR_INVALID_ARG;
+    if (use_sink && (mode < CSA_K0_ZERO || mode > CSA_K0_GIVEN)) return CSA_ERR_INVALID_ARG;
+    if ((long long)B * H * T == 0) {
+        *empty = true;
+        return CSA_OK;
+    }
+    if (!q || !k || !v || !out) return CSA_ERR_INVALID_ARG;
+    if (use_sink && mode == CSA_K0_GIVEN && (!k0 || !v0)) return CSA_ERR_INVALID_ARG;
+    if ((long long)B * H > 0x7fffffffLL || (long long)B * H * T > (1LL << 40))
+        return CSA_ERR_UNSUPPORTED;
+    return CSA_OK;
+}
+
+int device_ok() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CSA_ERR_NO_DEVICE;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return CSA_ERR_NO_DEVICE;
+    // The binary carries sm_103a code only.
+    if (major != 10 || minor != 3) return CSA_ERR_NO_DEVICE;
+    return CSA_OK;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+int forward_bf16(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+                 void *out, float *lse, int B, int H, int T, int d, float scale, int mode,
+                 bool continuous, csa_stream_t stream) {
+    bool empty;
+    int rc = check_common(q, k, v, k0, v0, out, B, H, T, d, scale, mode, continuous, &empty);
+    if (rc != CSA_OK || empty) return rc;
+    if (d > 256) return CSA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+        (lse && !aligned(lse, 4)))
+        return CSA_ERR_ALIGNMENT;
+    if (continuous && mode == CSA_K0_GIVEN && (!aligned(k0, 2) || !aligned(v0, 2)))
+        return CSA_ERR_ALIGNMENT;
+    if ((rc = device_ok()) != CSA_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (d == 64 || d == 128) {
+        if (scale < 0.0f) return CSA_ERR_UNSUPPORTED;
+        return csa_tc_forward(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, continuous, s);
+    }
+    return from_cuda(csa_simt_forward_bf16(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode,
+                                           continuous, s));
+}
+
+int forward_f32(const float *q, const float *k, const float *v, const float *k0, const float *v0,
+                float *out, float *lse, int B, int H, int T, int d, float scale, int mode,
+                bool continuous, csa_stream_t stream) {
+    bool empty;
+    int rc = check_common(q, k, v, k0, v0, out, B, H, T, d, scale, mode, continuous, &empty);
+    if (rc != CSA_OK || empty) return rc;
+    if (d > 256) return CSA_ERR_UNSUPPORTED;
+    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(out, 4) ||
+        (lse && !aligned(lse, 4)))
+        return CSA_ERR_ALIGNMENT;
+    if ((rc = device_ok()) != CSA_OK) return rc;
+    return from_cuda(csa_simt_forward_f32(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode,
+                                          continuous, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int csa_forward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+                void *out, float *lse, int B, int H, int T, int d, float scale, int k0_mode,
+                csa_stream_t stream) {
+    return forward_bf16(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, true, stream);
+}
+
+int csa_forward_f32(const float *q, const float *k, const float *v, const float *k0,
+                    const float *v0, float *out, float *lse, int B, int H, int T, int d,
+                    float scale, int k0_mode, csa_stream_t stream) {
+    return forward_f32(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, true, stream);
+}
+
+int csa_std_forward(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                    int H, int T, int d, float scale, csa_stream_t stream) {
+    return forward_bf16(q, k, v, nullptr, nullptr, out, lse, B, H, T, d, scale, CSA_K0_ZERO, false,
+                        stream);
+}
+
+int csa_std_forward_f32(const float *q, const float *k, const float *v, float *out, float *lse,
+                        int B, int H, int T, int d, float scale, csa_stream_t stream) {
+    return forward_f32(q, k, v, nullptr, nullptr, out, lse, B, H, T, d, scale, CSA_K0_ZERO, false,
+                       stream);
+}
+
+int csa_logphi2_eval(const float *x, float *y, int n, csa_stream_t stream) {
+    if (n < 0) return CSA_ERR_INVALID_ARG;
+    if (n == 0) return CSA_OK;
+    if (!x || !y) return CSA_ERR_INVALID_ARG;
+    int rc = device_ok();
+    if (rc != CSA_OK) return rc;
+    return from_cuda(csa_simt_logphi2_eval(x, y, n, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int csa_segment_weights_eval(const float *u0, const float *u1, float *right, float *left, int n,
+                             csa_stream_t stream) {
+    if (n < 0) return CSA_ERR_INVALID_ARG;
+    if (n == 0) return CSA_OK;
+    if (!u0 || !u1 || !right || !left) return CSA_ERR_INVALID_ARG;
+    int rc = device_ok();
+    if (rc != CSA_OK) return rc;
+    return from_cuda(csa_tc_segment_weights_eval(u0, u1, right, left, n,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int csa_device_status(void) {
+    int rc = device_ok();
+    if (rc != CSA_OK) return rc;
+    return csa_tc_take_status();
+}
+
+int csa_selftest_wait_timeout(unsigned timeout_us, csa_stream_t stream) {
+    if (timeout_us < 1 || timeout_us > 1000000u) return CSA_ERR_INVALID_ARG;
+    int rc = device_ok();
+    if (rc != CSA_OK) return rc;
+    return from_cuda(csa_tc_selftest_wait_timeout(timeout_us, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char *csa_status_string(int status) {
+    switch (status) {
+        case CSA_OK: return "ok";
+        case CSA_ERR_INVALID_ARG: return "invalid argument";
+        case CSA_ERR_UNSUPPORTED: return "unsupported shape or value";
+        case CSA_ERR_ALIGNMENT: return "misaligned pointer";
+        case CSA_ERR_CUDA: return "CUDA runtime error";
+        case CSA_ERR_TIMEOUT: return "device-side wait timed out";
+        case CSA_ERR_NO_DEVICE: return "no sm_103 device is current";
+        default: return "unknown status";
+    }
+}
+
+int csa_abi_version(void) { return CSA_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,27 @@
+// Launchers shared between the kernel translation units and the C ABI.
+// Arguments are validated by the C ABI before any of these is called.
+#pragma once
+
+#include <cuda_runtime.h>
+
+// CUDA-core kernels (csa_simt.cu).  continuous = false gives eq. (12).
+cudaError_t csa_simt_forward_f32(const float *q, const float *k, const float *v, const float *k0,
+                                 const float *v0, float *out, float *lse, int B, int H, int T,
+                                 int d, float scale, int mode, bool continuous,
+                                 cudaStream_t stream);
+cudaError_t csa_simt_forward_bf16(const void *q, const void *k, const void *v, const void *k0,
+                                  const void *v0, void *out, float *lse, int B, int H, int T,
+                                  int d, float scale, int mode, bool continuous,
+                                  cudaStream_t stream);
+cudaError_t csa_simt_logphi2_eval(const float *x, float *y, int n, cudaStream_t stream);
+
+// Tensor-core kernels (csa_tc.cu), d in {64, 128}, bf16.  Returns a CSA_*
+// status code (CSA_OK on success).
+int csa_tc_forward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+                   void *out, float *lse, int B, int H, int T, int d, float scale, int mode,
+                   bool continuous, cudaStream_t stream);
+cudaError_t csa_tc_segment_weights_eval(const float *u0, const float *u1, float *right,
+                                        float *left, int n, cudaStream_t stream);
+cudaError_t csa_tc_selftest_wait_timeout(unsigned timeout_us, cudaStream_t stream);
+// Reads and clears the device status word of csa_tc.cu on the current device.
+int csa_tc_take_status(void);

@@ -1,0 +1,169 @@
+/*
+ * csa.h - C ABI of libcsa.so: forward pass of causal Continuous Softmax
+ * Attention on one NVIDIA GB300 (sm_103a).
+ *
+ * The method: Jianlin Su, "Continuous Softmax Attention" (Scientific Spaces
+ * #11980).  Attention over the causal prefix is made continuous by linear
+ * interpolation of keys and values between integer positions (eq. (2), (3));
+ * the integrals close (eq. (4)-(7)) and reduce to a softmax over corrected
+ * logits (eq. (10), (11)):
+ *
+ *     a_{t,i} = scale * q_t . k_i                       i = 0..t
+ *     e^{b_{t,0}} = phi2(a_{t,1} - a_{t,0})
+ *     e^{b_{t,i}} = phi2(a_{t,i-1} - a_{t,i}) + phi2(a_{t,i+1} - a_{t,i})
+ *     e^{b_{t,t}} = phi2(a_{t,t-1} - a_{t,t})
+ *     o_t = sum_i e^{a+b} v_i / sum_i e^{a+b},   phi2(x) = (e^x - 1 - x)/x^2
+ *
+ * with an extra sink pair k_0, v_0 (section "Analysis of the Result": zero,
+ * a copy of the first token, or trainable).
+ *
+ * Common conventions for every attention entry point below
+ * ---------------------------------------------------------
+ *  Layout     q, k, v, out: contiguous row-major [B, H, T, d]; token r of the
+ *             arrays (0-based) is the page's t = r + 1, array key j is the
+ *             page's k_{j+1}.  k0, v0: contiguous [H, d] (one sink pair per
+ *             head, shared across the batch).  lse: contiguous float [B, H, T].
+ *  Memory     every pointer is DEVICE memory owned by the caller; the library
+ *             allocates nothing and keeps no pointer after the call returns.
+ *             out and lse must not overlap any input.
+ *  Stream     the work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *             legacy default stream) and the call returns without waiting.
+ *             Outputs are valid once the stream reaches that point.
+ *  Scale      logits are scale * q.k; the correction b is formed on the
+ *             scaled logits.  scale must be finite.
+ *  lse        natural-log normaliser: lse_t = log sum_i e^{a_{t,i}+b_{t,i}},
+ *             which equals log of eq. (2)'s denominator integral.  May be
+ *             NULL when not wanted.
+ *  Empty      B, H or T equal to 0 is a valid empty problem: CSA_OK, nothing
+ *             is launched.
+ *  Errors     the return value is CSA_OK (0) or one of the negative codes
+ *             below.  Argument errors are detected on the host before any
+ *             launch, and nothing is enqueued.  CSA_ERR_CUDA reports a launch
+ *             failure (cudaGetLastError); asynchronous kernel faults surface,
+ *             as usual in CUDA, on the next synchronising call.  Device-side
+ *             bounded waits that expire set a sticky status word readable
+ *             with csa_device_status().
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *csa_stream_t;
+
+/* Choice of the extra pair k_0, v_0 ("Analysis of the Result", last
+ * paragraph: all zeros; k_0 = k_1, v_0 = v_1; or trainable). */
+typedef enum {
+    CSA_K0_ZERO = 0,       /* k_0 = v_0 = 0 (the page's experiments)       */
+    CSA_K0_COPY_FIRST = 1, /* k_0 = k_1, v_0 = v_1 of the same (b, h)       */
+    CSA_K0_GIVEN = 2       /* k0, v0 supplied per head, [H, d]              */
+} csa_k0_mode;
+
+enum {
+    CSA_OK = 0,
+    CSA_ERR_INVALID_ARG = -1, /* NULL pointer, negative size, d < 1,
+                                 non-finite scale, bad mode, k0/v0 NULL in
+                                 CSA_K0_GIVEN                                 */
+    CSA_ERR_UNSUPPORTED = -2, /* shape or value outside what a kernel
+                                 supports (see each entry point)              */
+    CSA_ERR_ALIGNMENT = -3,   /* a pointer is not aligned as required         */
+    CSA_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed         */
+    CSA_ERR_TIMEOUT = -5,     /* a device-side bounded wait expired           */
+    CSA_ERR_NO_DEVICE = -6    /* no usable sm_103 device is current           */
+};
+
+/*
+ * csa_forward - continuous attention, bf16 inputs, tensor-core path.
+ *   Defines: eq. (10)/(11) of "Continuous Softmax Attention" ("Assembly and
+ *   Simplification"), which equals eq. (2) ("Problem Statement").
+ *   q, k, v, k0, v0: bf16 (__nv_bfloat16); out: bf16; lse: float.
+ *   Accumulation and the correction b are computed in fp32.
+ *   d = 64 or 128 runs the tcgen05/TMA kernel; any other 1 <= d <= 256 runs
+ *   the CUDA-core kernel.  d > 256: CSA_ERR_UNSUPPORTED.  scale < 0 on the
+ *   tensor-core kernel: CSA_ERR_UNSUPPORTED.
+ *   q, k, v, out must be 16-byte aligned (CSA_ERR_ALIGNMENT otherwise).
+ *   k0, v0 are read only in CSA_K0_GIVEN mode and may be NULL otherwise.
+ */
+int csa_forward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+                void *out, float *lse, int B, int H, int T, int d, float scale, int k0_mode,
+                csa_stream_t stream);
+
+/*
+ * csa_forward_f32 - continuous attention, fp32 inputs and outputs, computed
+ *   in fp32 on CUDA cores (no TF32), with b formed in the log domain by a
+ *   stable log phi2 (series near 0, logarithmic form for large |x|, combined
+ *   by logaddexp).  Same definition and conventions as csa_forward;
+ *   1 <= d <= 256.  All pointers 4-byte aligned.
+ */
+int csa_forward_f32(const float *q, const float *k, const float *v, const float *k0,
+                    const float *v0, float *out, float *lse, int B, int H, int T, int d,
+                    float scale, int k0_mode, csa_stream_t stream);
+
+/*
+ * csa_std_forward - standard causal softmax attention (b = 0, no sink),
+ *   bf16 inputs, tensor-core path.
+ *   Defines: eq. (12) of "Continuous Softmax Attention" ("Analysis of the
+ *   Result"), the same as softmax(q k^T * scale + M) v with the causal mask M
+ *   of "Attention, from the softmax up" ("The one line").
+ *   lse_t = log sum_{i=1}^t e^{a_{t,i}}.  Same layout, alignment and d rules
+ *   as csa_forward.
+ */
+int csa_std_forward(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                    int H, int T, int d, float scale, csa_stream_t stream);
+
+/* csa_std_forward_f32 - eq. (12) in fp32 on CUDA cores; 1 <= d <= 256. */
+int csa_std_forward_f32(const float *q, const float *k, const float *v, float *out, float *lse,
+                        int B, int H, int T, int d, float scale, csa_stream_t stream);
+
+/*
+ * csa_logphi2_eval - y[i] = log phi2(x[i]) with the library's fp32 device
+ *   function (phi2 of eq. (6), "Preliminaries").  x, y: device float arrays
+ *   of n elements (n >= 0).  A test hook for the numerics of b.
+ */
+int csa_logphi2_eval(const float *x, float *y, int n, csa_stream_t stream);
+
+/*
+ * csa_segment_weights_eval - the tensor-core kernel's fp32 evaluation of
+ *   one interval's two end weights, for tests.  For each i, with
+ *   x = u1[i] - u0[i] in natural-log units and p = e^{u}:
+ *       right[i] = p0 * phi2(x)    (the share of interval (u0,u1) that eq. (9)
+ *       left[i]  = p1 * phi2(-x)    moves onto its left and right key)
+ *   u0, u1: device float arrays (u <= 0 expected, as after subtracting a
+ *   running max); right, left: device float outputs; n >= 0.
+ */
+int csa_segment_weights_eval(const float *u0, const float *u1, float *right, float *left, int n,
+                             csa_stream_t stream);
+
+/*
+ * csa_device_status - reads and clears the library's sticky device status
+ *   word of the current device: CSA_OK, or CSA_ERR_TIMEOUT if a kernel's
+ *   bounded wait expired since the last read (that kernel then skipped the
+ *   rest of its work and its outputs are undefined).  Synchronises the
+ *   device.  Returns CSA_ERR_CUDA if the read itself fails.
+ */
+int csa_device_status(void);
+
+/*
+ * csa_selftest_wait_timeout - launches one block whose thread waits on an
+ *   mbarrier that nothing ever completes, with a time limit of timeout_us
+ *   microseconds (1..10^6).  The wait gives up, the kernel records
+ *   CSA_ERR_TIMEOUT in the status word and returns normally; the context
+ *   stays usable.  Exercises the bounded-wait path of the kernels without
+ *   any fault.
+ */
+int csa_selftest_wait_timeout(unsigned timeout_us, csa_stream_t stream);
+
+/* Human-readable text for a status code (never NULL, static storage). */
+const char *csa_status_string(int status);
+
+/* ABI version of this header (bumped on incompatible change). */
+int csa_abi_version(void);
+#define CSA_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA_H_ */

@@ -1,0 +1,94 @@
+"""Host-side checks of the C ABI (no GPU needed, nothing is launched).
+
+The library must load, export every function include/csa.h declares, and
+reject bad arguments with the documented codes before touching the device."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+from continuous_softmax_attention_gb300 import _lib as L
+
+FAKE = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+NULL = None
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(L.LIB_PATH):
+        from continuous_softmax_attention_gb300 import build
+
+        build.build()
+    return L.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = L.header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True)
+    exported = {line.split()[-1] for line in out.stdout.splitlines() if line.strip()}
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    assert lib.csa_abi_version() == 1
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert L.status_string(code) not in ("", "unknown status")
+    assert L.status_string(123) == "unknown status"
+
+
+def fwd(lib, *, q=FAKE, k=FAKE, v=FAKE, k0=NULL, v0=NULL, out=FAKE, lse=NULL, B=1, H=1, T=8, d=64,
+        scale=0.125, mode=0):
+    return lib.csa_forward(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, None)
+
+
+def test_argument_validation(lib):
+    assert fwd(lib, q=NULL) == L.CSA_ERR_INVALID_ARG
+    assert fwd(lib, out=NULL) == L.CSA_ERR_INVALID_ARG
+    assert fwd(lib, B=-1) == L.CSA_ERR_INVALID_ARG
+    assert fwd(lib, d=0) == L.CSA_ERR_INVALID_ARG
+    assert fwd(lib, mode=3) == L.CSA_ERR_INVALID_ARG
+    assert fwd(lib, mode=2) == L.CSA_ERR_INVALID_ARG  # given sink without k0/v0
+    assert fwd(lib, scale=float("nan")) == L.CSA_ERR_INVALID_ARG
+    assert fwd(lib, scale=float("inf")) == L.CSA_ERR_INVALID_ARG
+    assert fwd(lib, d=300) == L.CSA_ERR_UNSUPPORTED
+    assert fwd(lib, q=ctypes.c_void_p(4098)) == L.CSA_ERR_ALIGNMENT
+    assert fwd(lib, out=ctypes.c_void_p(4104)) == L.CSA_ERR_ALIGNMENT
+
+
+def test_empty_problems_are_ok(lib):
+    # nothing to compute: success without any pointer or device
+    assert fwd(lib, q=NULL, k=NULL, v=NULL, out=NULL, B=0) == L.CSA_OK
+    assert fwd(lib, q=NULL, k=NULL, v=NULL, out=NULL, T=0) == L.CSA_OK
+    assert lib.csa_std_forward(NULL, NULL, NULL, NULL, NULL, 2, 0, 5, 64, 0.1, None) == L.CSA_OK
+    assert lib.csa_logphi2_eval(NULL, NULL, 0, None) == L.CSA_OK
+    assert lib.csa_logphi2_eval(NULL, NULL, -1, None) == L.CSA_ERR_INVALID_ARG
+
+
+def test_std_and_f32_validation(lib):
+    assert lib.csa_std_forward(FAKE, FAKE, NULL, FAKE, NULL, 1, 1, 4, 64, 0.1, None) == L.CSA_ERR_INVALID_ARG
+    assert lib.csa_forward_f32(FAKE, FAKE, FAKE, NULL, NULL, FAKE, NULL, 1, 1, 4, 257, 0.1, 0, None) == L.CSA_ERR_UNSUPPORTED
+    assert lib.csa_forward_f32(ctypes.c_void_p(4097), FAKE, FAKE, NULL, NULL, FAKE, NULL, 1, 1, 4, 16, 0.1, 0, None) == L.CSA_ERR_ALIGNMENT
+    assert lib.csa_selftest_wait_timeout(0, None) == L.CSA_ERR_INVALID_ARG
+    assert lib.csa_selftest_wait_timeout(2000000, None) == L.CSA_ERR_INVALID_ARG
+
+
+def test_no_device_is_reported(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # valid arguments: the call reaches the device check and stops there
+    assert fwd(lib) == L.CSA_ERR_NO_DEVICE
+    assert lib.csa_device_status() == L.CSA_ERR_NO_DEVICE
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(L, "_lib", None)
+    monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        L.load()

@@ -1,0 +1,80 @@
+"""The method's evaluation workloads at full size, in the launch configuration
+the benchmark times, checked against the oracle: whole heads where the
+oracle is quick, and otherwise rows sampled at every tile edge plus random
+rows of every head (the oracle computes those one by one)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import continuous_softmax_attention_gb300 as csa
+import oracle
+from continuous_softmax_attention_gb300.inputs import WORKLOADS, workload_inputs
+from gpu_util import assert_close, boundary_rows, np64, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _sampled(x, o, lse, mode, scale, rows_per_head, std=False, seed=0):
+    B, H, T, d = x["q"].shape
+    rng = np.random.default_rng(seed)
+    picks = []
+    edges = boundary_rows(T)
+    for b in range(B):
+        for h in range(H):
+            chosen = set(rng.choice(edges, size=min(len(edges), rows_per_head), replace=False).tolist())
+            chosen.update(rng.integers(0, T, size=4).tolist())
+            picks += [(b, h, int(r)) for r in sorted(chosen)]
+    rows = oracle.flat_rows(B, H, T, picks)
+    ro, rl = oracle.forward_rows(x["q"], x["k"], x["v"], rows, x["k0"], x["v0"], scale=scale,
+                                 mode=mode, std=std)
+    og = np64(o).reshape(-1, d)[rows]
+    lg = np64(lse).reshape(-1)[rows]
+    return assert_close(og, lg, ro, rl, "bf16", "sampled rows")
+
+
+def _full_heads(x, o, lse, mode, scale, heads, std=False):
+    for (b, h) in heads:
+        sub = {k: v[b:b + 1, h:h + 1] if v.dim() == 4 else v[h:h + 1] for k, v in x.items()}
+        if std:
+            ro, rl = oracle.std_forward(sub["q"], sub["k"], sub["v"], scale=scale)
+        else:
+            ro, rl = oracle.forward(sub["q"], sub["k"], sub["v"], sub["k0"], sub["v0"], scale=scale,
+                                    mode=mode)
+        assert_close(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], ro, rl, "bf16", f"head {b},{h}")
+
+
+def _run(name):
+    w = WORKLOADS[name]
+    x = workload_inputs(name)
+    g = to_dev(x)
+    scale = 1.0 / math.sqrt(w.d)
+    mode = w.modes[0]
+    o, lse = csa.forward(g["q"], g["k"], g["v"], g["k0"], g["v0"], mode=mode, scale=scale)
+    torch.cuda.synchronize()
+    assert csa.device_status() == 0
+    return w, x, g, o, lse, mode, scale
+
+
+def test_mid_workload():
+    """B=4, H=16, T=2048, d=128, RoPE on q and k, zero sink."""
+    w, x, g, o, lse, mode, scale = _run("mid")
+    _full_heads(x, o, lse, mode, scale, [(0, 0), (3, 15)])
+    _sampled(x, o, lse, mode, scale, rows_per_head=12, seed=1)
+
+
+def test_headline_workload():
+    """B=1, H=32, T=8192, d=128, zero sink; and the standard kernel on it."""
+    w, x, g, o, lse, mode, scale = _run("headline")
+    _full_heads(x, o, lse, mode, scale, [(0, 31)])
+    _sampled(x, o, lse, mode, scale, rows_per_head=8, seed=2)
+    so, sl = csa.std_forward(g["q"], g["k"], g["v"], scale=scale)
+    torch.cuda.synchronize()
+    _sampled(x, so, sl, mode, scale, rows_per_head=6, std=True, seed=3)
+
+
+def test_long_workload():
+    """B=1, H=8, T=32768, d=64, given per-head k0, v0 (trainable-sink mode)."""
+    w, x, g, o, lse, mode, scale = _run("long")
+    _sampled(x, o, lse, mode, scale, rows_per_head=24, seed=4)
