@@ -57,6 +57,8 @@ namespace {
 __device__ int g_tc_status;  // sticky status word of this file's kernels
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+// Wait for PV(j) to complete before issuing S(j+1) into the TMEM it reads.
+constexpr bool kWaitPvBeforeS = false;
 constexpr int kThreads = 320;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -122,18 +124,20 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
 
 // One interval's two end weights (see the file comment), times (ln 2)^2.
 // X = u_right - u_left in log2 units, p = 2^u.
+// For |X| >= 1/16 the closed form: its error, from the independent rounding
+// of the two exponentials divided by X^2, stays below 4e-4 relative.  Below,
+// the power series of phi2 to first order, whose truncation error is
+// (ln2 X)^2 / 12 < 1.6e-4.  Both are under the bf16 rounding of P (2^-9).
 __device__ __forceinline__ void seg_weights(float X, float p0, float p1, float &R, float &L) {
-    constexpr float C0 = 0.2402265069591007f;     // (ln2)^2 / 2!
-    constexpr float C1 = 0.055504108664821576f;   // (ln2)^3 / 3!
-    constexpr float C2 = 0.009618129107628477f;   // (ln2)^4 / 4!
-    constexpr float C3 = 0.0013333558146428441f;  // (ln2)^5 / 5!
-    constexpr float kTau = 0.25f;                 // |X| below: power series
+    constexpr float C0 = 0.2402265069591007f;    // (ln2)^2 / 2!
+    constexpr float C1 = 0.055504108664821576f;  // (ln2)^3 / 3!
+    constexpr float kTau = 0.0625f;
     const float rx = rcp_approx(X);
-    const float sig = (p1 - p0) * rx;              // S * ln2
-    const float rc = fmaf(-p0, kLn2, sig) * rx;    // R * (ln2)^2
-    const float lc = fmaf(sig, kLn2, -rc);         // L * (ln2)^2
-    const float rs = p0 * fmaf(X, fmaf(X, fmaf(X, C3, C2), C1), C0);
-    const float ls = p1 * fmaf(X, fmaf(X, fmaf(-X, C3, C2), -C1), C0);
+    const float sig = (p1 - p0) * rx;            // S * ln2
+    const float rc = fmaf(-p0, kLn2, sig) * rx;  // R * (ln2)^2
+    const float lc = fmaf(sig, kLn2, -rc);       // L * (ln2)^2
+    const float rs = p0 * fmaf(X, C1, C0);
+    const float ls = p1 * fmaf(X, -C1, C0);
     const bool small = fabsf(X) < kTau;
     R = small ? rs : rc;
     L = small ? ls : lc;
@@ -154,6 +158,190 @@ __device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
             return;
         }
     }
+}
+
+// Per-row online-softmax state of one softmax thread.
+struct RowState {
+    float k2;      // scale * log2(e)
+    float m_run;   // running max of the logits, log2 units
+    float l_run;   // fp32 sum of the weights (gives lse)
+    float l_bf;    // sum of the weights as rounded to bf16 for PV (normalises o)
+    float carry;   // L share of the next tile's first key (continuous kernel)
+    float w_sink;  // weight of the given sink pair (k0, v0 supplied)
+    float s_sink;  // q . k0 of the given sink pair
+};
+
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t &r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
+}
+
+// One 32-column chunk of weights of the continuous kernel.  sv[0..32] are
+// the raw logits q.k of columns cbase..cbase+32; Lc is the L share of column
+// cbase coming from the left.  Produces w[0..31] (e^{a+b-m} * (ln2)^2),
+// returns in Lc the L share of column cbase+32, and in L31 that of cbase+31.
+template <bool MASKED>
+__device__ __forceinline__ void cont_chunk(const float (&sv)[33], float k2, float nm, int cbase,
+                                           int c_last, float &Lc, float &L31, float (&w)[32]) {
+    float u[33], pe[33], L[33], R[32];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const float2 t = __ffma2_rn(make_float2(sv[i], sv[i + 1]), make_float2(k2, k2),
+                                    make_float2(nm, nm));
+        u[i] = t.x;
+        u[i + 1] = t.y;
+    }
+    u[32] = fmaf(sv[32], k2, nm);
+#pragma unroll
+    for (int i = 0; i < 33; ++i) pe[i] = ex2_approx(u[i]);
+    L[0] = Lc;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        float Ri, Li;
+        seg_weights(u[i + 1] - u[i], pe[i], pe[i + 1], Ri, Li);
+        if (MASKED) {
+            // interval (c, c+1) exists for this row only if c+1 <= its last key
+            const bool seg_ok = cbase + i + 1 <= c_last;
+            Ri = seg_ok ? Ri : 0.0f;
+            Li = seg_ok ? Li : 0.0f;
+        }
+        R[i] = Ri;
+        L[i + 1] = Li;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const float2 t = __fadd2_rn(make_float2(L[i], L[i + 1]), make_float2(R[i], R[i + 1]));
+        w[i] = t.x;
+        w[i + 1] = t.y;
+    }
+    L31 = L[31];
+    Lc = L[32];
+}
+
+// Softmax of one S tile held in TMEM at tS for this thread's row: tile max,
+// lazy rescale of the running state, weights, P (bf16) written back over the
+// first 64 columns of S.  Returns whether the running max moved (alpha is
+// then the factor the accumulated O must be scaled by).
+template <bool CONT, bool MASKED>
+__device__ __forceinline__ bool softmax_tile(uint32_t tS, RowState &st, int c_last, int sink,
+                                             float &alpha) {
+    // ---- pass 1: max over the valid columns
+    float mx;
+    {
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + 32 * cc, sr[cc]);
+        tmem_wait_ld();
+        float s0 = __uint_as_float(sr[0][0]);
+        if (CONT && sink == 1) s0 = __uint_as_float(sr[0][1]);
+        if (CONT && sink == 2) s0 = st.s_sink;
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+            float v0 = c == 0 ? s0 : __uint_as_float(sr[c >> 5][c & 31]);
+            float v1 = __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]);
+            if (MASKED) {
+                v0 = c <= c_last ? v0 : -INFINITY;
+                v1 = c + 1 <= c_last ? v1 : -INFINITY;
+            }
+            a[(c >> 1) & 7] = fmax3f(a[(c >> 1) & 7], v0, v1);
+        }
+        mx = fmax3f(fmax3f(a[0], a[1], a[2]), fmax3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+    }
+    const float mt = (!MASKED || c_last >= 0) ? mx * st.k2 : -INFINITY;
+    alpha = 1.0f;
+    const bool grow = mt > st.m_run + 8.0f;
+    if (grow) {
+        alpha = ex2_approx(st.m_run - mt);
+        st.m_run = mt;
+        st.l_run *= alpha;
+        st.l_bf *= alpha;
+        st.carry *= alpha;
+        st.w_sink *= alpha;
+    }
+    const float nm = -st.m_run;
+    const float k2 = st.k2;
+    // ---- pass 2: weights, 32 columns at a time
+    float2 lsum = make_float2(0.0f, 0.0f), bsum = make_float2(0.0f, 0.0f);
+    float Lc = st.carry;
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+        uint32_t a[32];
+        tmem_ld32(tS + 32 * k, a);
+        uint32_t nx = 0;
+        if (CONT && k < 3) tmem_ld1(tS + 32 * k + 32, nx);
+        tmem_wait_ld();
+        float w[32];
+        if (CONT) {
+            float sv[33];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(a[i]);
+            sv[32] = k < 3 ? __uint_as_float(nx) : sv[31];
+            if (k == 0 && sink == 1) sv[0] = sv[1];
+            if (k == 0 && sink == 2) sv[0] = st.s_sink;
+            float L31;
+            cont_chunk<MASKED>(sv, k2, nm, 32 * k, c_last, Lc, L31, w);
+            if (k == 3) {
+                Lc = L31;   // L share of the halo key = next tile's first key
+                w[31] = 0.0f;
+            }
+            if (k == 0 && sink == 1) {  // v_0 = v_1: the sink's weight lands on key 1
+                w[1] += w[0];
+                w[0] = 0.0f;
+            }
+            if (k == 0 && sink == 2) {  // w_0 * v0 is added in fp32 at the end
+                st.w_sink = w[0];
+                w[0] = 0.0f;
+                st.l_run += st.w_sink;
+                st.l_bf += st.w_sink;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float2 t = __ffma2_rn(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])),
+                                            make_float2(k2, k2), make_float2(nm, nm));
+                w[i] = ex2_approx(t.x);
+                w[i + 1] = ex2_approx(t.y);
+            }
+            if (MASKED) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) w[i] = 32 * k + i <= c_last ? w[i] : 0.0f;
+            }
+        }
+        uint32_t pk[16];
+        float2 ls2 = make_float2(0.0f, 0.0f), bs2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            const uint32_t pr = pack_bf16x2(w[i], w[i + 1]);
+            pk[i >> 1] = pr;
+            if ((i & 2) == 0)
+                lsum = __fadd2_rn(lsum, make_float2(w[i], w[i + 1]));
+            else
+                ls2 = __fadd2_rn(ls2, make_float2(w[i], w[i + 1]));
+            if (CONT) {
+                const float2 rb = make_float2(__uint_as_float(pr << 16), __uint_as_float(pr & 0xffff0000u));
+                if ((i & 2) == 0)
+                    bsum = __fadd2_rn(bsum, rb);
+                else
+                    bs2 = __fadd2_rn(bs2, rb);
+            }
+        }
+        lsum = __fadd2_rn(lsum, ls2);
+        if (CONT) bsum = __fadd2_rn(bsum, bs2);
+        tmem_st16(tS + 16 * k, pk);
+    }
+    tmem_wait_st();
+    st.carry = Lc;
+    st.l_run += lsum.x + lsum.y;
+    if (CONT) st.l_bf += bsum.x + bsum.y;
+    return grow;
 }
 
 template <int D, bool CONT>
@@ -312,9 +500,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     if (!(ok = issue_pv(qt, j))) break;
                     if (j + 1 < ntiles[qt]) {
-                        // S(j+1) overwrites the TMEM that PV(j) reads as P.
-                        if (!(ok = wait_bar(BAR(C::kBarODone + qt), j & 1, abort_flag))) break;
-                        tc_fence_after();
+                        // S(j+1) overwrites the TMEM that PV(j) reads as P; both
+                        // are tcgen05.mma issued in order by this thread.
+                        if (kWaitPvBeforeS) {
+                            if (!(ok = wait_bar(BAR(C::kBarODone + qt), j & 1, abort_flag))) break;
+                            tc_fence_after();
+                        }
                         if (!(ok = issue_s(qt, j + 1))) break;
                     }
                 }
@@ -336,11 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + C::col_s(qt);
         const uint32_t tO = tmem + lane_off + C::col_o(qt);
-        const float k2 = p.k2;
-        // l_run: fp32 sum of the weights (for lse); l_bf: sum of the weights as
-        // rounded to bf16 for the PV product (normalises o consistently).
-        float m_run = -INFINITY, l_run = 0.0f, l_bf = 0.0f, carry = 0.0f, w_sink = 0.0f,
-              s_sink = 0.0f;
+        RowState st;
+        st.k2 = p.k2;
+        st.m_run = -INFINITY;
+        st.l_run = st.l_bf = st.carry = st.w_sink = st.s_sink = 0.0f;
         bool ok = n > 0;
         if (CONT && ok && p.mode == 2) {
             ok = __all_sync(0xffffffffu, wait_bar(BAR(C::kBarQ), 0, abort_flag));
@@ -363,121 +553,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        __bfloat162float(k0h[cc * 64 + kc * 8 + e]), acc);
                     }
                 }
-                s_sink = acc;
+                st.s_sink = acc;
             }
         }
         for (int j = 0; ok && j < n; ++j) {
             ok = __all_sync(0xffffffffu, wait_bar(BAR(C::kBarSFull + qt), j & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + 32 * cc, sr[cc]);
-            tmem_wait_ld();
-            float s[128];
-#pragma unroll
-            for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
-
             // last valid column of this row, and whether the tile needs masks
             const int c_last = CONT ? r + 1 - 127 * j : r - 128 * j;
             const bool masked = CONT ? (127 * j + 127 > row0[qt] + 1) : (128 * j + 127 > row0[qt]);
-            if (CONT && j == 0) {
-                if (p.mode == 1) s[0] = s[1];
-                else if (p.mode == 2) s[0] = s_sink;
-            }
-            float mx = -INFINITY;
-            if (!masked) {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c <= c_last) mx = fmaxf(mx, s[c]);
-            }
-            const float mt = c_last >= 0 ? mx * k2 : -INFINITY;
-            float alpha = 1.0f;
-            const bool grow = mt > m_run + 8.0f;
-            if (grow) {
-                alpha = ex2_approx(m_run - mt);
-                m_run = mt;
-                l_run *= alpha;
-                l_bf *= alpha;
-                carry *= alpha;
-                w_sink *= alpha;
-            }
-            const float nm = -m_run;
-            float w[128];
-            if (CONT) {
-                float u_prev = fmaf(s[0], k2, nm);
-                float p_prev = ex2_approx(u_prev);
-                float Lc = carry;
-                if (!masked) {
-#pragma unroll
-                    for (int c = 0; c < 127; ++c) {
-                        const float u1 = fmaf(s[c + 1], k2, nm);
-                        const float p1 = ex2_approx(u1);
-                        float R, Ln;
-                        seg_weights(u1 - u_prev, p_prev, p1, R, Ln);
-                        w[c] = Lc + R;
-                        Lc = Ln;
-                        u_prev = u1;
-                        p_prev = p1;
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 127; ++c) {
-                        const float u1 = fmaf(s[c + 1], k2, nm);
-                        const float p1 = ex2_approx(u1);
-                        float R, Ln;
-                        seg_weights(u1 - u_prev, p_prev, p1, R, Ln);
-                        const bool seg_ok = c + 1 <= c_last;
-                        R = seg_ok ? R : 0.0f;
-                        Ln = seg_ok ? Ln : 0.0f;
-                        w[c] = c <= c_last ? Lc + R : 0.0f;
-                        Lc = Ln;
-                        u_prev = u1;
-                        p_prev = p1;
-                    }
-                }
-                carry = Lc;
-                w[127] = 0.0f;
-            } else {
-                if (!masked) {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c) w[c] = ex2_approx(fmaf(s[c], k2, nm));
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        w[c] = c <= c_last ? ex2_approx(fmaf(s[c], k2, nm)) : 0.0f;
-                }
-            }
-            if (CONT && j == 0) {
-                if (p.mode == 1) {
-                    w[1] += w[0];  // v_0 = v_1: the sink's weight lands on key 1
-                    w[0] = 0.0f;
-                } else if (p.mode == 2) {
-                    w_sink = w[0];  // w_0 * v0 is added in fp32 at the end
-                    w[0] = 0.0f;
-                    l_run += w_sink;
-                    l_bf += w_sink;
-                }
-            }
-            float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            float b4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            uint32_t pk[2][32];
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const uint32_t pr = pack_bf16x2(w[2 * i], w[2 * i + 1]);
-                pk[i >> 5][i & 31] = pr;
-                l4[(2 * i) & 3] += w[2 * i];
-                l4[(2 * i + 1) & 3] += w[2 * i + 1];
-                b4[i & 3] += __uint_as_float(pr << 16) + __uint_as_float(pr & 0xffff0000u);
-            }
-            l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-            l_bf += (b4[0] + b4[1]) + (b4[2] + b4[3]);
-            tmem_st32(tS, pk[0]);
-            tmem_st32(tS + 32, pk[1]);
-            tmem_wait_st();
+            const int sink = (CONT && j == 0) ? p.mode : 0;
+            float alpha;
+            bool grow;
+            if (masked)
+                grow = softmax_tile<CONT, true>(tS, st, c_last, sink, alpha);
+            else
+                grow = softmax_tile<CONT, false>(tS, st, c_last, sink, alpha);
             // Rescale O when this row's max moved (after PV(j-1) finished).
             const bool need_o = grow && j > 0;
             if (__any_sync(0xffffffffu, need_o)) {
@@ -504,7 +596,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, wait_bar(BAR(C::kBarODone + qt), (n - 1) & 1, abort_flag));
             if (ok) {
                 tc_fence_after();
-                const float inv_l = 1.0f / l_bf;
+                // the continuous kernel divides by the bf16-rounded weight sum that
+                // fed the PV product; the standard one by the fp32 sum
+                const float inv_l = 1.0f / (CONT ? st.l_bf : st.l_run);
                 const bool store = r < T;
                 __nv_bfloat16 *orow = p.out + ((size_t)bh * T + (size_t)(store ? r : 0)) * D;
                 const __nv_bfloat16 *v0h = p.v0 + (size_t)(bh % p.H) * D;
@@ -517,7 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         float x = __uint_as_float(o[e]);
-                        if (CONT && p.mode == 2) x = fmaf(w_sink, __bfloat162float(v0h[32 * cc + e]), x);
+                        if (CONT && p.mode == 2)
+                            x = fmaf(st.w_sink, __bfloat162float(v0h[32 * cc + e]), x);
                         val[e] = x * inv_l;
                     }
                     uint32_t pk[16];
@@ -532,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (store && p.lse)
                     p.lse[(size_t)bh * T + r] =
-                        (m_run + log2f(l_run)) * kLn2 + (CONT ? kLseShift : 0.0f);
+                        (st.m_run + log2f(st.l_run)) * kLn2 + (CONT ? kLseShift : 0.0f);
             }
         }
     }

@@ -1,0 +1,44 @@
+"""Runs the forward kernels a few times at one shape (for profilers).
+
+    python -m continuous_softmax_attention_gb300.run_case --B 1 --H 24 --T 8192 --d 128
+
+Inputs come from the seeded generator; each iteration launches the
+continuous kernel once and, unless --no-std, the standard kernel once.
+"""
+from __future__ import annotations
+
+import argparse
+import math
+
+import torch
+
+import continuous_softmax_attention_gb300 as csa
+from continuous_softmax_attention_gb300.inputs import make_inputs
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--B", type=int, default=1)
+    ap.add_argument("--H", type=int, default=24)
+    ap.add_argument("--T", type=int, default=8192)
+    ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--mode", type=int, default=0)
+    ap.add_argument("--iters", type=int, default=2)
+    ap.add_argument("--no-std", action="store_true")
+    a = ap.parse_args()
+    x = make_inputs(a.B, a.H, a.T, a.d, "bf16", seed=0)
+    g = {k: v.cuda() for k, v in x.items()}
+    scale = 1.0 / math.sqrt(a.d)
+    for _ in range(a.iters):
+        o, lse = csa.forward(g["q"], g["k"], g["v"], g["k0"], g["v0"], mode=a.mode, scale=scale)
+        if not a.no_std:
+            csa.std_forward(g["q"], g["k"], g["v"], scale=scale)
+    torch.cuda.synchronize()
+    st = csa.device_status()
+    print(f"ok status={st} o_mean={o.float().abs().mean().item():.5f}")
+    if st != 0:
+        raise SystemExit(1)
+
+
+if __name__ == "__main__":
+    main()

@@ -46,12 +46,15 @@ def test_segment_weights_against_phi2():
     p0, p1 = np.exp(u0.astype(np.float64)), np.exp(u1.astype(np.float64))
     rr = np.array([a * oracle.phi2(s) for a, s in zip(p0, xx)])
     rl = np.array([b * oracle.phi2(-s) for b, s in zip(p1, xx)])
-    # relative to the interval's larger end value (=1): what the softmax sees
+    # Bound: the kernel's closed form loses ~1.4e-6/X^2 (X in log2 units) to the
+    # rounding of the two exponentials, and below |X| = 1/16 it switches to a
+    # first-order series with error (ln2 X)^2/12; both stay under 4e-4
+    # relative, below the 2^-9 rounding of the bf16 P these weights become.
     assert np.isfinite(r).all() and np.isfinite(l_).all()
-    assert np.abs(r - rr).max() < 3e-5, np.abs(r - rr).max()
-    assert np.abs(l_ - rl).max() < 3e-5, np.abs(l_ - rl).max()
+    assert np.abs(r - rr).max() < 3e-4, np.abs(r - rr).max()
+    assert np.abs(l_ - rl).max() < 3e-4, np.abs(l_ - rl).max()
     big = rr > 1e-3
-    assert (np.abs(r - rr)[big] / rr[big]).max() < 1e-4
+    assert (np.abs(r - rr)[big] / rr[big]).max() < 1e-3
 
 
 def test_bounded_wait_times_out_without_fault():
