@@ -123,24 +123,27 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
 }
 
 // One interval's two end weights (see the file comment), times (ln 2)^2.
-// X = u_right - u_left in log2 units, p = 2^u.
-// For |X| >= 1/16 the closed form: its error, from the independent rounding
-// of the two exponentials divided by X^2, stays below 4e-4 relative.  Below,
-// the power series of phi2 to first order, whose truncation error is
-// (ln2 X)^2 / 12 < 1.6e-4.  Both are under the bf16 rounding of P (2^-9).
+// X = u_right - u_left in log2 units, p = 2^u, x = X ln2 the logit step.
+// Closed form (|X| >= 1/16):
+//     sig = (p1 - p0)/X = S ln2,  R = (sig - p0 ln2)/X,  L = sig ln2 - R.
+// Its error, the independent rounding of the two exponentials divided by
+// X^2, stays below 4e-4 relative.  For |X| < 1/16 the same three lines run
+// with other coefficients, giving the trapezoid value of S and the
+// first-order expansion of phi2:
+//     sig = (p0 + p1) ln2/2,  R = (ln2)^2 (2 p0 + p1)/6,  L = (ln2)^2 (p0 + 2 p1)/6,
+// which match p0 phi2(x) and p1 phi2(-x) to (x^2)/12 relative (< 1.6e-4).
+// Both errors are below the 2^-9 rounding of the bf16 P these weights become.
 __device__ __forceinline__ void seg_weights(float X, float p0, float p1, float &R, float &L) {
-    constexpr float C0 = 0.2402265069591007f;    // (ln2)^2 / 2!
-    constexpr float C1 = 0.055504108664821576f;  // (ln2)^3 / 3!
     constexpr float kTau = 0.0625f;
     const float rx = rcp_approx(X);
-    const float sig = (p1 - p0) * rx;            // S * ln2
-    const float rc = fmaf(-p0, kLn2, sig) * rx;  // R * (ln2)^2
-    const float lc = fmaf(sig, kLn2, -rc);       // L * (ln2)^2
-    const float rs = p0 * fmaf(X, C1, C0);
-    const float ls = p1 * fmaf(X, -C1, C0);
     const bool small = fabsf(X) < kTau;
-    R = small ? rs : rc;
-    L = small ? ls : lc;
+    const float a1 = small ? 1.0f : -1.0f;
+    const float f1 = small ? 0.5f * kLn2 : rx;
+    const float a2 = fmaf(a1, 0.75f * kLn2, -0.25f * kLn2);  // ln2/2 or -ln2
+    const float f2 = small ? kLn2 / 3.0f : rx;
+    const float sig = fmaf(p0, a1, p1) * f1;
+    R = fmaf(p0, a2, sig) * f2;
+    L = fmaf(sig, kLn2, -R);
 }
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
@@ -179,6 +182,43 @@ __device__ __forceinline__ float fmax3f(float a, float b, float c) {
 
 __device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t &r) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
+}
+
+// tcgen05.wait::ld that also names the destination registers of the loads
+// it waits for, so that no use of them can be scheduled before it.
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[N]);
+template <>
+__device__ __forceinline__ void tmem_wait_ld_regs<32>(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_wait_ld_regs<33>(uint32_t (&r)[33]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31]), "+r"(r[32])
+                 :
+                 : "memory");
+}
+
+// Issues the TMEM loads of S chunk k (32 columns, plus the next column for
+// the continuous kernel's right neighbour); completed by tmem_wait_ld_regs.
+template <bool CONT>
+__device__ __forceinline__ void load_chunk(uint32_t tS, int k, uint32_t (&b)[33]) {
+    tmem_ld32(tS + 32 * k, *reinterpret_cast<uint32_t(*)[32]>(&b[0]));
+    if (CONT && k < 3) tmem_ld1(tS + 32 * k + 32, b[32]);
 }
 
 // One 32-column chunk of weights of the continuous kernel.  sv[0..32] are
@@ -236,7 +276,8 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, RowState &st, int c_la
         uint32_t sr[4][32];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + 32 * cc, sr[cc]);
-        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tmem_wait_ld_regs<32>(sr[cc]);
         float s0 = __uint_as_float(sr[0][0]);
         if (CONT && sink == 1) s0 = __uint_as_float(sr[0][1]);
         if (CONT && sink == 2) s0 = st.s_sink;
@@ -271,25 +312,19 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, RowState &st, int c_la
     // ---- pass 2: weights, 32 columns at a time
     float2 lsum = make_float2(0.0f, 0.0f), bsum = make_float2(0.0f, 0.0f);
     float Lc = st.carry;
-#pragma unroll 1
-    for (int k = 0; k < 4; ++k) {
-        uint32_t a[32];
-        tmem_ld32(tS + 32 * k, a);
-        uint32_t nx = 0;
-        if (CONT && k < 3) tmem_ld1(tS + 32 * k + 32, nx);
-        tmem_wait_ld();
+    auto chunk = [&](int k, uint32_t (&a)[33]) {
         float w[32];
         if (CONT) {
             float sv[33];
 #pragma unroll
             for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(a[i]);
-            sv[32] = k < 3 ? __uint_as_float(nx) : sv[31];
+            sv[32] = k < 3 ? __uint_as_float(a[32]) : sv[31];
             if (k == 0 && sink == 1) sv[0] = sv[1];
             if (k == 0 && sink == 2) sv[0] = st.s_sink;
             float L31;
             cont_chunk<MASKED>(sv, k2, nm, 32 * k, c_last, Lc, L31, w);
             if (k == 3) {
-                Lc = L31;   // L share of the halo key = next tile's first key
+                Lc = L31;  // L share of the halo key = next tile's first key
                 w[31] = 0.0f;
             }
             if (k == 0 && sink == 1) {  // v_0 = v_1: the sink's weight lands on key 1
@@ -336,6 +371,14 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, RowState &st, int c_la
         lsum = __fadd2_rn(lsum, ls2);
         if (CONT) bsum = __fadd2_rn(bsum, bs2);
         tmem_st16(tS + 16 * k, pk);
+    };
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+        uint32_t b[33];
+        b[32] = 0u;
+        load_chunk<CONT>(tS, k, b);
+        tmem_wait_ld_regs<33>(b);
+        chunk(k, b);
     }
     tmem_wait_st();
     st.carry = Lc;
@@ -490,6 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit(BAR(C::kBarODone + qt));
                 return true;
             };
+            // For each key tile j and query tile: wait P(j), PV(j), then S(j+1).
+            // K tile j+1 is released after its S products, V tile j after its PV.
             for (int qt = 0; qt < 2 && ok; ++qt)
                 if (ntiles[qt] > 0) ok = issue_s(qt, 0);
             if (ok) tc_commit(BAR(C::kBarKEmpty + 0));
