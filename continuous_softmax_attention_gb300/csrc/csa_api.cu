@@ -63,7 +63,8 @@ int forward_bf16(const void *q, const void *k, const void *v, const void *k0, co
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (d == 64 || d == 128) {
         if (scale < 0.0f) return CSA_ERR_UNSUPPORTED;
-        return csa_tc_forward(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, continuous, s);
+        if (continuous) return csa_tc_forward(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, s);
+        return csa_tc_std_forward(q, k, v, out, lse, B, H, T, d, scale, s);
     }
     return from_cuda(csa_simt_forward_bf16(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode,
                                            continuous, s));
@@ -135,7 +136,9 @@ int csa_segment_weights_eval(const float *u0, const float *u1, float *right, flo
 int csa_device_status(void) {
     int rc = device_ok();
     if (rc != CSA_OK) return rc;
-    return csa_tc_take_status();
+    const int a = csa_tc_take_status();
+    const int b = csa_tc_std_take_status();
+    return a != CSA_OK ? a : b;
 }
 
 int csa_selftest_wait_timeout(unsigned timeout_us, csa_stream_t stream) {

@@ -15,13 +15,18 @@ cudaError_t csa_simt_forward_bf16(const void *q, const void *k, const void *v, c
                                   cudaStream_t stream);
 cudaError_t csa_simt_logphi2_eval(const float *x, float *y, int n, cudaStream_t stream);
 
-// Tensor-core kernels (csa_tc.cu), d in {64, 128}, bf16.  Returns a CSA_*
-// status code (CSA_OK on success).
+// Tensor-core kernels, d in {64, 128}, bf16.  Return a CSA_* status code
+// (CSA_OK on success).  Continuous attention (csa_tc.cu):
 int csa_tc_forward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
                    void *out, float *lse, int B, int H, int T, int d, float scale, int mode,
-                   bool continuous, cudaStream_t stream);
+                   cudaStream_t stream);
+// Standard causal attention, eq. (12) (csa_tc_std.cu):
+int csa_tc_std_forward(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                       int H, int T, int d, float scale, cudaStream_t stream);
 cudaError_t csa_tc_segment_weights_eval(const float *u0, const float *u1, float *right,
                                         float *left, int n, cudaStream_t stream);
 cudaError_t csa_tc_selftest_wait_timeout(unsigned timeout_us, cudaStream_t stream);
-// Reads and clears the device status word of csa_tc.cu on the current device.
+// Read and clear the device status words of csa_tc.cu / csa_tc_std.cu on
+// the current device.
 int csa_tc_take_status(void);
+int csa_tc_std_take_status(void);

@@ -1,102 +1,113 @@
-// Tensor-core forward kernels for sm_103a (bf16 inputs, d = 64 or 128):
-//  * continuous attention, eq. (10)/(11) of Jianlin Su, "Continuous Softmax
-//    Attention" ("Assembly and Simplification");
-//  * standard causal attention, eq. (12) of the same page ("Analysis of the
-//    Result"), built from the same skeleton with b = 0 and no sink.
+// Tensor-core forward kernel of causal continuous attention for sm_103a:
+// eq. (10)/(11) of Jianlin Su, "Continuous Softmax Attention" ("Assembly
+// and Simplification"), bf16 inputs, d = 64 or 128, fp32 accumulation.
 //
-// Work split.  One CTA owns two 128-row query tiles of one (b, h) and walks
-// the key/value tiles up to their diagonal.  Warps:
-//   0-3  softmax warpgroup of query tile 0 (one thread = one query row)
-//   4-7  softmax warpgroup of query tile 1
-//   8    TMA producer (lane 0)
+// Work split.  One CTA owns one 128-row query tile of one (b, h) and walks
+// the key/value tiles up to its diagonal (heaviest query tiles launch first).
+// Warps:
+//   0-7  softmax: warp w owns rows 32*(w%4).. (its TMEM lane quarter) and,
+//        with w/4, the column half 0..63 or 64..127 of S
+//   8    TMA producer (lane 0; all lanes write the constant ones block once)
 //   9    TMEM allocator and tcgen05.mma issuer (lane 0)
-// Shared memory holds both Q tiles, a K ring and a V ring, all 128B-swizzled
-// 64-column boxes written by TMA.  Tensor memory (512 columns) holds
-// S0 | S1 | O0 | O1 in fp32; the bf16 P of a tile overwrites the first 64
-// columns of its own S and feeds the PV product straight from TMEM.
+// Shared memory holds the Q tile, a K ring and a V ring of 128B-swizzled
+// 64-column boxes written by TMA.  Each V stage has one more box holding a
+// column of ones, so the PV product (N = d + 16) also accumulates, in O
+// column d, the row sum of exactly the bf16 P values it used.
+// Tensor memory (512 columns): S buffer 0 | S buffer 1 | O (d + 16 columns).
+// S is double-buffered: the tensor core computes PV(j) and S(j+2) while the
+// softmax works on S(j+1).  P (bf16) overwrites columns of its own S that
+// are no longer read (0..31 and 80..111) and is the A operand of the PV
+// product straight from TMEM.
 //
-// The continuous kernel's halo.  b_{t,i} needs the logit of the key to the
-// right of i.  Key tiles are therefore loaded at a stride of 127 rows: an S
-// tile covers 128 consecutive keys of the extended sequence (the sink
-// first), its last column is the first key of the next tile, and that
-// column's P is 0.  Tile j starts at array row 127*j - 1; for j = 0 this row
-// is -1, which TMA fills with zeros: the zero sink pair k_0 = v_0 = 0 comes
-// for free, and the copy-first and given modes only replace the first logit
-// (and, for given v_0, add w_0 * v_0 to the output at the end).
+// The halo for b.  b_{t,i} needs the logit of the key to the right of i.
+// Key tiles are loaded at a stride of 127 rows: an S tile covers 128
+// consecutive keys of the extended sequence (the sink first), its last
+// column is the first key of the next tile, and that column's P is 0.  Tile
+// j starts at array row 127*j - 1; for j = 0 this row is -1, which TMA fills
+// with zeros: the zero sink pair k_0 = v_0 = 0 comes for free, and the
+// copy-first and given modes only replace the first logit (and, for given
+// v_0, add w_0 * v_0 to the output at the end).
 //
 // The weights.  With the running max m (log2 units) and u = a*log2(e) - m,
 // p = 2^u, each interval between neighbouring keys contributes
 //   R = p_left * phi2(x)  to its left key and  L = p_right * phi2(-x)  to its
-// right key (x the logit step), which is the regrouping of eq. (9); a key's
-// weight e^{a+b-m} is L + R of its two intervals, one-sided at both ends.
-// R and L follow from the interval integral S = (p_right - p_left)/x by
+// right key (x the logit step), the regrouping of eq. (9); a key's weight
+// e^{a+b-m} is L + R of its two intervals, one-sided at both ends.  R and L
+// follow from the interval integral S = (p_right - p_left)/x by
 // R = (S - p_left)/x and L = S - R, with a power series for small steps.
 // All weights carry a common factor (ln 2)^2, which cancels in o and is
 // removed from lse.
 //
-// Every mbarrier wait is bounded in time; on expiry the kernel records
-// CSA_ERR_TIMEOUT, every role skips its remaining work, the MMA issuer waits
-// for its own MMAs, the producer waits for its own copies, and TMEM is freed.
+// The two column halves of a row exchange their partial maxima, the L share
+// that crosses into the next tile, and their final sums through shared
+// memory, synchronised by an mbarrier.  Every mbarrier wait is bounded in
+// time; on expiry the kernel records CSA_ERR_TIMEOUT, every role skips its
+// remaining work, the MMA issuer waits for its own MMAs, the producer waits
+// for its own copies, and TMEM is freed.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "csa.h"
-#include "csa_device.cuh"
 #include "csa_internal.h"
+#include "csa_tc_common.cuh"
 
-using namespace csa_dev;
+using namespace csa_tc;
 
 namespace {
 
 __device__ int g_tc_status;  // sticky status word of this file's kernels
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
-// Wait for PV(j) to complete before issuing S(j+1) into the TMEM it reads.
-constexpr bool kWaitPvBeforeS = false;
-constexpr int kThreads = 320;
-constexpr float kLn2 = 0.69314718055994531f;
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+constexpr int kThreads = 32 * 10;
 // -log((ln 2)^2): removes the common weight factor from lse
 constexpr float kLseShift = 0.7330258411633287f;
 
 template <int D>
 struct TcCfg {
-    static constexpr int kChunks = D / 64;          // 64-column boxes per tile
-    static constexpr int kChunkBytes = 128 * 128;   // 128 rows x 128 bytes
+    static constexpr int kChunks = D / 64;  // 64-column boxes per tile
     static constexpr int kTileBytes = kChunks * kChunkBytes;
+    static constexpr int kVStageBytes = kTileBytes + kChunkBytes;  // values + ones box
+    static constexpr int kN = D + 16;                              // PV width
     static constexpr int kStagesK = D == 128 ? 2 : 3;
     static constexpr int kStagesV = D == 128 ? 2 : 3;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+    static constexpr int kOffK = kOffQ + kTileBytes;
     static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
-    static constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
+    static constexpr int kOffBar = kOffV + kStagesV * kVStageBytes;
     // barrier indices
     static constexpr int kBarQ = 0;
     static constexpr int kBarKFull = 1;
     static constexpr int kBarKEmpty = kBarKFull + kStagesK;
     static constexpr int kBarVFull = kBarKEmpty + kStagesK;
     static constexpr int kBarVEmpty = kBarVFull + kStagesV;
-    static constexpr int kBarSFull = kBarVEmpty + kStagesV;  // [2]
-    static constexpr int kBarPFull = kBarSFull + 2;          // [2]
-    static constexpr int kBarODone = kBarPFull + 2;          // [2]
-    static constexpr int kBarDrain = kBarODone + 2;
-    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kBarSFull = kBarVEmpty + kStagesV;  // [2] one per S buffer
+    static constexpr int kBarPFull = kBarSFull + 2;
+    static constexpr int kBarODone = kBarPFull + 1;
+    static constexpr int kBarDrain = kBarODone + 1;
+    static constexpr int kBarX = kBarDrain + 1;  // half-to-half exchange
+    static constexpr int kNumBars = kBarX + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
-    // TMEM columns: S0 | S1 | O0 | O1
-    __device__ static constexpr uint32_t col_s(int qt) { return 128u * (uint32_t)qt; }
-    __device__ static constexpr uint32_t col_o(int qt) { return 256u + (uint32_t)(D * qt); }
+    // exchange buffers between the two column halves of the query tile:
+    //   xmax   [2 slots][2 halves][128 rows]  partial row maxima
+    //   xcarry [2 slots][128 rows]            L share carried to the next tile
+    //   xfin   [2 halves][128 rows][2]        final fp32 sum, sink weight
+    static constexpr int kOffXMax = kOffMisc + 16;
+    static constexpr int kOffXCarry = kOffXMax + 2 * 2 * 128 * 4;
+    static constexpr int kOffXFin = kOffXCarry + 2 * 128 * 4;
+    static constexpr int kSmemBytes = kOffXFin + 2 * 128 * 2 * 4 + 1024;  // + slack to align the base
+    // TMEM columns: S buffer 0 | S buffer 1 | O
+    __device__ static constexpr uint32_t col_s(int b) { return 128u * (uint32_t)b; }
+    static constexpr uint32_t kColO = 256u;
 };
 
 struct TcParams {
     int B, H, T;
-    int num_pairs;
+    int num_qtiles;
     float k2;  // scale * log2(e)
     int mode;
     const __nv_bfloat16 *k0;
@@ -105,25 +116,16 @@ struct TcParams {
     float *lse;
 };
 
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A
-// and B, A K-major, B K-major or MN-major, shape M x N.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+__device__ __forceinline__ bool wait_c(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    return wait_bar(bar, parity, abort_flag, &g_tc_status);
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle.
-__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= 1ull << 46;  // descriptor version for this architecture
-    d |= 2ull << 61;  // 128-byte swizzle
-    return d;
-}
+// ------------------------------------------------------------- weights
+// |X| below this (log2 units) takes the small-step coefficients.
+constexpr float kTau = 0.0625f;
 
-// One interval's two end weights (see the file comment), times (ln 2)^2.
-// X = u_right - u_left in log2 units, p = 2^u, x = X ln2 the logit step.
+// One interval's two end weights, times (ln 2)^2.  X = u_right - u_left in
+// log2 units, p = 2^u, x = X ln2 the logit step.
 // Closed form (|X| >= 1/16):
 //     sig = (p1 - p0)/X = S ln2,  R = (sig - p0 ln2)/X,  L = sig ln2 - R.
 // Its error, the independent rounding of the two exponentials divided by
@@ -134,7 +136,6 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
 // which match p0 phi2(x) and p1 phi2(-x) to (x^2)/12 relative (< 1.6e-4).
 // Both errors are below the 2^-9 rounding of the bf16 P these weights become.
 __device__ __forceinline__ void seg_weights(float X, float p0, float p1, float &R, float &L) {
-    constexpr float kTau = 0.0625f;
     const float rx = rcp_approx(X);
     const bool small = fabsf(X) < kTau;
     const float a1 = small ? 1.0f : -1.0f;
@@ -146,85 +147,10 @@ __device__ __forceinline__ void seg_weights(float X, float p0, float p1, float &
     L = fmaf(sig, kLn2, -R);
 }
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
-    return mbar_wait_bounded(bar, parity, abort_flag, &g_tc_status, kWaitLimitNs);
-}
-
-// Wait that ignores the abort flag: used only to let in-flight copies and
-// MMAs finish before the block exits.
-__device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            *(volatile int *)&g_tc_status = kStatusTimeout;
-            return;
-        }
-    }
-}
-
-// Per-row online-softmax state of one softmax thread.
-struct RowState {
-    float k2;      // scale * log2(e)
-    float m_run;   // running max of the logits, log2 units
-    float l_run;   // fp32 sum of the weights (gives lse)
-    float l_bf;    // sum of the weights as rounded to bf16 for PV (normalises o)
-    float carry;   // L share of the next tile's first key (continuous kernel)
-    float w_sink;  // weight of the given sink pair (k0, v0 supplied)
-    float s_sink;  // q . k0 of the given sink pair
-};
-
-__device__ __forceinline__ float fmax3f(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
-__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t &r) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
-}
-
-// tcgen05.wait::ld that also names the destination registers of the loads
-// it waits for, so that no use of them can be scheduled before it.
-template <int N>
-__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[N]);
-template <>
-__device__ __forceinline__ void tmem_wait_ld_regs<32>(uint32_t (&r)[32]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
-                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
-                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
-                   "+r"(r[30]), "+r"(r[31])
-                 :
-                 : "memory");
-}
-template <>
-__device__ __forceinline__ void tmem_wait_ld_regs<33>(uint32_t (&r)[33]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
-                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
-                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
-                   "+r"(r[30]), "+r"(r[31]), "+r"(r[32])
-                 :
-                 : "memory");
-}
-
-// Issues the TMEM loads of S chunk k (32 columns, plus the next column for
-// the continuous kernel's right neighbour); completed by tmem_wait_ld_regs.
-template <bool CONT>
-__device__ __forceinline__ void load_chunk(uint32_t tS, int k, uint32_t (&b)[33]) {
-    tmem_ld32(tS + 32 * k, *reinterpret_cast<uint32_t(*)[32]>(&b[0]));
-    if (CONT && k < 3) tmem_ld1(tS + 32 * k + 32, b[32]);
-}
-
-// One 32-column chunk of weights of the continuous kernel.  sv[0..32] are
-// the raw logits q.k of columns cbase..cbase+32; Lc is the L share of column
-// cbase coming from the left.  Produces w[0..31] (e^{a+b-m} * (ln2)^2),
-// returns in Lc the L share of column cbase+32, and in L31 that of cbase+31.
+// One 32-column chunk of weights.  sv[0..32] are the raw logits q.k of
+// columns cbase..cbase+32; Lc is the L share of column cbase coming from the
+// left.  Produces w[0..31] (e^{a+b-m} * (ln2)^2), returns in Lc the L share
+// of column cbase+32, and in L31 that of cbase+31.
 template <bool MASKED>
 __device__ __forceinline__ void cont_chunk(const float (&sv)[33], float k2, float nm, int cbase,
                                            int c_last, float &Lc, float &L31, float (&w)[32]) {
@@ -263,131 +189,106 @@ __device__ __forceinline__ void cont_chunk(const float (&sv)[33], float k2, floa
     Lc = L[32];
 }
 
-// Softmax of one S tile held in TMEM at tS for this thread's row: tile max,
-// lazy rescale of the running state, weights, P (bf16) written back over the
-// first 64 columns of S.  Returns whether the running max moved (alpha is
-// then the factor the accumulated O must be scaled by).
-template <bool CONT, bool MASKED>
-__device__ __forceinline__ bool softmax_tile(uint32_t tS, RowState &st, int c_last, int sink,
-                                             float &alpha) {
-    // ---- pass 1: max over the valid columns
-    float mx;
-    {
-        uint32_t sr[4][32];
+// Per-row online-softmax state of one softmax thread.
+struct RowState {
+    float k2;      // scale * log2(e)
+    float m_run;   // running max of the logits, log2 units
+    float l_run;   // fp32 sum of this half's weights (gives lse)
+    float w_sink;  // weight of the given sink pair (k0, v0 supplied)
+    float s_sink;  // q . k0 of the given sink pair
+};
+
+// Pass 1 of a half tile: max of the raw logits over this warp's 64 columns
+// (valid columns only; column 0 replaced by the sink logit if any).
+template <bool MASKED>
+__device__ __forceinline__ float half_max(const uint32_t (&a)[2][32], int half, int c_last,
+                                          float s0) {
+    float m[4];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + 32 * cc, sr[cc]);
+    for (int i = 0; i < 4; ++i) m[i] = -INFINITY;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_wait_ld_regs<32>(sr[cc]);
-        float s0 = __uint_as_float(sr[0][0]);
-        if (CONT && sink == 1) s0 = __uint_as_float(sr[0][1]);
-        if (CONT && sink == 2) s0 = st.s_sink;
-        float a[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-            float v0 = c == 0 ? s0 : __uint_as_float(sr[c >> 5][c & 31]);
-            float v1 = __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]);
-            if (MASKED) {
-                v0 = c <= c_last ? v0 : -INFINITY;
-                v1 = c + 1 <= c_last ? v1 : -INFINITY;
-            }
-            a[(c >> 1) & 7] = fmax3f(a[(c >> 1) & 7], v0, v1);
+    for (int c = 0; c < 64; c += 2) {
+        const int col = 64 * half + c;
+        float v0 = c == 0 ? s0 : __uint_as_float(a[c >> 5][c & 31]);
+        float v1 = __uint_as_float(a[(c + 1) >> 5][(c + 1) & 31]);
+        if (MASKED) {
+            v0 = col <= c_last ? v0 : -INFINITY;
+            v1 = col + 1 <= c_last ? v1 : -INFINITY;
         }
-        mx = fmax3f(fmax3f(a[0], a[1], a[2]), fmax3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+        m[(c >> 1) & 3] = fmax3f(m[(c >> 1) & 3], v0, v1);
     }
-    const float mt = (!MASKED || c_last >= 0) ? mx * st.k2 : -INFINITY;
-    alpha = 1.0f;
-    const bool grow = mt > st.m_run + 8.0f;
-    if (grow) {
-        alpha = ex2_approx(st.m_run - mt);
-        st.m_run = mt;
-        st.l_run *= alpha;
-        st.l_bf *= alpha;
-        st.carry *= alpha;
-        st.w_sink *= alpha;
-    }
-    const float nm = -st.m_run;
+    return fmax3f(m[0], m[1], fmaxf(m[2], m[3]));
+}
+
+// TMEM column where the P of 32 keys of S (16 packed columns) is written:
+// half 0's keys 0..63 go to columns 0..31 of S, half 1's keys 64..127 to
+// 80..111: columns that by then only their own warp has read.
+__device__ __forceinline__ uint32_t p_col(int k) { return k < 2 ? 16u * k : 80u + 16u * (k - 2); }
+
+// Pass 2 of a half tile: weights of this warp's 64 keys, P written to TMEM,
+// fp32 sum accumulated.  a: the half's 64 logits; nb: column 64 for half 0
+// (right neighbour of its last key), column 63 for half 1 (left neighbour
+// of its first key).  Lc enters as the L share of the half's first key
+// coming from the left and leaves (half 1) as that of the halo key, the
+// next tile's first key.
+template <bool MASKED>
+__device__ __forceinline__ void half_weights(uint32_t tS, const uint32_t (&a)[2][32], uint32_t nb,
+                                             RowState &st, int half, int c_last, int sink,
+                                             float nm, float &Lc) {
     const float k2 = st.k2;
-    // ---- pass 2: weights, 32 columns at a time
-    float2 lsum = make_float2(0.0f, 0.0f), bsum = make_float2(0.0f, 0.0f);
-    float Lc = st.carry;
-    auto chunk = [&](int k, uint32_t (&a)[33]) {
-        float w[32];
-        if (CONT) {
-            float sv[33];
+    if (half == 1) {
+        // interval (63, 64) gives key 64 its share from the left
+        const float u0 = fmaf(__uint_as_float(nb), k2, nm);
+        const float u1 = fmaf(__uint_as_float(a[0][0]), k2, nm);
+        float R, L;
+        seg_weights(u1 - u0, ex2_approx(u0), ex2_approx(u1), R, L);
+        Lc = (!MASKED || 64 <= c_last) ? L : 0.0f;
+    }
+    float2 lsum = make_float2(0.0f, 0.0f), ls2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(a[i]);
-            sv[32] = k < 3 ? __uint_as_float(a[32]) : sv[31];
-            if (k == 0 && sink == 1) sv[0] = sv[1];
-            if (k == 0 && sink == 2) sv[0] = st.s_sink;
-            float L31;
-            cont_chunk<MASKED>(sv, k2, nm, 32 * k, c_last, Lc, L31, w);
-            if (k == 3) {
-                Lc = L31;  // L share of the halo key = next tile's first key
-                w[31] = 0.0f;
-            }
-            if (k == 0 && sink == 1) {  // v_0 = v_1: the sink's weight lands on key 1
-                w[1] += w[0];
-                w[0] = 0.0f;
-            }
-            if (k == 0 && sink == 2) {  // w_0 * v0 is added in fp32 at the end
-                st.w_sink = w[0];
-                w[0] = 0.0f;
-                st.l_run += st.w_sink;
-                st.l_bf += st.w_sink;
-            }
-        } else {
+    for (int kk = 0; kk < 2; ++kk) {
+        const int k = 2 * half + kk;
+        float sv[33];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float2 t = __ffma2_rn(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])),
-                                            make_float2(k2, k2), make_float2(nm, nm));
-                w[i] = ex2_approx(t.x);
-                w[i + 1] = ex2_approx(t.y);
-            }
-            if (MASKED) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) w[i] = 32 * k + i <= c_last ? w[i] : 0.0f;
-            }
+        for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(a[kk][i]);
+        if (kk == 0)
+            sv[32] = __uint_as_float(a[1][0]);
+        else
+            sv[32] = half == 0 ? __uint_as_float(nb) : sv[31];  // column 64, or unused
+        if (k == 0 && sink == 1) sv[0] = sv[1];       // k_0 = k_1
+        if (k == 0 && sink == 2) sv[0] = st.s_sink;   // given k_0
+        float w[32], L31;
+        cont_chunk<MASKED>(sv, k2, nm, 32 * k, c_last, Lc, L31, w);
+        if (k == 3) {
+            Lc = L31;  // L share of the halo key = next tile's first key
+            w[31] = 0.0f;
+        }
+        if (k == 0 && sink == 1) {  // v_0 = v_1: the sink's weight lands on key 1
+            w[1] += w[0];
+            w[0] = 0.0f;
+        }
+        if (k == 0 && sink == 2) {  // w_0 * v0 is added in fp32 at the end
+            st.w_sink = w[0];
+            w[0] = 0.0f;
+            st.l_run += st.w_sink;
         }
         uint32_t pk[16];
-        float2 ls2 = make_float2(0.0f, 0.0f), bs2 = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-            const uint32_t pr = pack_bf16x2(w[i], w[i + 1]);
-            pk[i >> 1] = pr;
+            pk[i >> 1] = pack_bf16x2(w[i], w[i + 1]);
             if ((i & 2) == 0)
                 lsum = __fadd2_rn(lsum, make_float2(w[i], w[i + 1]));
             else
                 ls2 = __fadd2_rn(ls2, make_float2(w[i], w[i + 1]));
-            if (CONT) {
-                const float2 rb = make_float2(__uint_as_float(pr << 16), __uint_as_float(pr & 0xffff0000u));
-                if ((i & 2) == 0)
-                    bsum = __fadd2_rn(bsum, rb);
-                else
-                    bs2 = __fadd2_rn(bs2, rb);
-            }
         }
-        lsum = __fadd2_rn(lsum, ls2);
-        if (CONT) bsum = __fadd2_rn(bsum, bs2);
-        tmem_st16(tS + 16 * k, pk);
-    };
-#pragma unroll 1
-    for (int k = 0; k < 4; ++k) {
-        uint32_t b[33];
-        b[32] = 0u;
-        load_chunk<CONT>(tS, k, b);
-        tmem_wait_ld_regs<33>(b);
-        chunk(k, b);
+        tmem_st16(tS + p_col(k), pk);
     }
     tmem_wait_st();
-    st.carry = Lc;
+    lsum = __fadd2_rn(lsum, ls2);
     st.l_run += lsum.x + lsum.y;
-    if (CONT) st.l_bf += bsum.x + bsum.y;
-    return grow;
 }
 
-template <int D, bool CONT>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_forward_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -407,20 +308,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BH = p.B * p.H;
     const int bh = (int)(blockIdx.x % (unsigned)BH);
-    const int pair = p.num_pairs - 1 - (int)(blockIdx.x / (unsigned)BH);
+    const int qtile = p.num_qtiles - 1 - (int)(blockIdx.x / (unsigned)BH);
     const int T = p.T;
-    int row0[2], ntiles[2];
-#pragma unroll
-    for (int qt = 0; qt < 2; ++qt) {
-        row0[qt] = pair * 256 + qt * 128;
-        if (row0[qt] >= T) {
-            ntiles[qt] = 0;
-        } else {
-            const int rl = min(row0[qt] + 127, T - 1);
-            ntiles[qt] = CONT ? (rl + 1) / 127 + 1 : rl / 128 + 1;
-        }
-    }
-    const int nj = max(ntiles[0], ntiles[1]);
+    const int row0 = qtile * 128;
+    const int n = (min(row0 + 127, T - 1) + 1) / 127 + 1;  // key tiles of this query tile
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(C::kBarQ), 1);
@@ -432,16 +323,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(C::kBarVFull + s), 1);
             mbar_init(BAR(C::kBarVEmpty + s), 1);
         }
-        for (int qt = 0; qt < 2; ++qt) {
-            mbar_init(BAR(C::kBarSFull + qt), 1);
-            mbar_init(BAR(C::kBarPFull + qt), 128);
-            mbar_init(BAR(C::kBarODone + qt), 1);
-        }
+        mbar_init(BAR(C::kBarSFull + 0), 1);
+        mbar_init(BAR(C::kBarSFull + 1), 1);
+        mbar_init(BAR(C::kBarPFull), 256);
+        mbar_init(BAR(C::kBarODone), 1);
         mbar_init(BAR(C::kBarDrain), 1);
+        mbar_init(BAR(C::kBarX), 256);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == kWarpProducer) {
+        // The ones box of every V stage: in swizzled row r (a key of the
+        // tile), logical 16-byte chunk 0 holds (1, 0, .., 0) and chunk 1
+        // zeros, so B columns d..d+15 of the PV product are (1, 0, .., 0).
+        for (int s = 0; s < NSV; ++s) {
+            uint8_t *ones = smem + C::kOffV + s * C::kVStageBytes + C::kTileBytes;
+            for (int r = lane; r < 128; r += 32) {
+                *reinterpret_cast<uint4 *>(ones + r * 128 + ((0 ^ (r & 7)) << 4)) =
+                    make_uint4(0x3F80u, 0u, 0u, 0u);  // bf16 1.0 in element 0
+                *reinterpret_cast<uint4 *>(ones + r * 128 + ((1 ^ (r & 7)) << 4)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == kWarpMma) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -450,135 +356,115 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 8) {
+    if (warp >= 8) {
+      if (warp == kWarpProducer) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0 && nj > 0) {
+        if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            uint32_t qbytes = 0;
-            for (int qt = 0; qt < 2; ++qt)
-                if (ntiles[qt] > 0) qbytes += C::kTileBytes;
-            mbar_arrive_expect_tx(BAR(C::kBarQ), qbytes);
-            for (int qt = 0; qt < 2; ++qt)
-                if (ntiles[qt] > 0)
-                    for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(sQ + qt * C::kTileBytes + c * C::kChunkBytes, &tm_q, 64 * c,
-                                    row0[qt], bh, BAR(C::kBarQ));
+            mbar_arrive_expect_tx(BAR(C::kBarQ), C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(sQ + c * kChunkBytes, &tm_q, 64 * c, row0, bh, BAR(C::kBarQ));
             int issued_k = 0, issued_v = 0;
-            for (int j = 0; j < nj; ++j) {
-                const int krow = CONT ? 127 * j - 1 : 128 * j;
+            for (int j = 0; j < n; ++j) {
+                const int krow = 127 * j - 1;
                 const int sk = j % NSK;
-                if (!wait_bar(BAR(C::kBarKEmpty + sk), ((j / NSK) & 1) ^ 1, abort_flag)) break;
+                if (!wait_c(BAR(C::kBarKEmpty + sk), ((j / NSK) & 1) ^ 1, abort_flag)) break;
                 mbar_arrive_expect_tx(BAR(C::kBarKFull + sk), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sK + sk * C::kTileBytes + c * C::kChunkBytes, &tm_k, 64 * c, krow,
-                                bh, BAR(C::kBarKFull + sk));
+                    tma_load_3d(sK + sk * C::kTileBytes + c * kChunkBytes, &tm_k, 64 * c, krow, bh,
+                                BAR(C::kBarKFull + sk));
                 issued_k = j + 1;
                 const int sv = j % NSV;
-                if (!wait_bar(BAR(C::kBarVEmpty + sv), ((j / NSV) & 1) ^ 1, abort_flag)) break;
+                if (!wait_c(BAR(C::kBarVEmpty + sv), ((j / NSV) & 1) ^ 1, abort_flag)) break;
                 mbar_arrive_expect_tx(BAR(C::kBarVFull + sv), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sV + sv * C::kTileBytes + c * C::kChunkBytes, &tm_v, 64 * c, krow,
+                    tma_load_3d(sV + sv * C::kVStageBytes + c * kChunkBytes, &tm_v, 64 * c, krow,
                                 bh, BAR(C::kBarVFull + sv));
                 issued_v = j + 1;
             }
             // Let every copy this thread issued land before the block can exit.
-            wait_bar_drain(BAR(C::kBarQ), 0);
+            wait_bar_drain(BAR(C::kBarQ), 0, &g_tc_status);
             for (int j = max(0, issued_k - NSK); j < issued_k; ++j)
-                wait_bar_drain(BAR(C::kBarKFull + j % NSK), (j / NSK) & 1);
+                wait_bar_drain(BAR(C::kBarKFull + j % NSK), (j / NSK) & 1, &g_tc_status);
             for (int j = max(0, issued_v - NSV); j < issued_v; ++j)
-                wait_bar_drain(BAR(C::kBarVFull + j % NSV), (j / NSV) & 1);
+                wait_bar_drain(BAR(C::kBarVFull + j % NSV), (j / NSV) & 1, &g_tc_status);
         }
         __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0 && nj > 0) {
+        if (lane == 0) {
             constexpr uint32_t kIdescS = make_idesc(128, 128, false);
-            constexpr uint32_t kIdescO = make_idesc(128, D, true);
-            bool ok = wait_bar(BAR(C::kBarQ), 0, abort_flag);
+            constexpr uint32_t kIdescO = make_idesc(128, C::kN, true);
+            bool ok = wait_c(BAR(C::kBarQ), 0, abort_flag);
             tc_fence_after();
-            int k_seen = -1, v_seen = -1;
-            auto issue_s = [&](int qt, int j) -> bool {
-                if (k_seen < j) {
-                    if (!wait_bar(BAR(C::kBarKFull + j % NSK), (j / NSK) & 1, abort_flag))
-                        return false;
-                    k_seen = j;
-                    tc_fence_after();
-                }
-                const uint32_t qb = sQ + qt * C::kTileBytes;
+            // S(j) = Q K_j^T into S buffer j % 2; K tile j is released once done
+            auto issue_s = [&](int j) -> bool {
+                if (!wait_c(BAR(C::kBarKFull + j % NSK), (j / NSK) & 1, abort_flag)) return false;
+                tc_fence_after();
                 const uint32_t kb = sK + (j % NSK) * C::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                    tc_mma_ss(tmem + C::col_s(qt), make_sdesc(qb + off, 16, 1024),
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    tc_mma_ss(tmem + C::col_s(j & 1), make_sdesc(sQ + off, 16, 1024),
                               make_sdesc(kb + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(BAR(C::kBarSFull + qt));
+                tc_commit(BAR(C::kBarSFull + (j & 1)));
+                tc_commit(BAR(C::kBarKEmpty + j % NSK));
                 return true;
             };
-            auto issue_pv = [&](int qt, int j) -> bool {
-                if (v_seen < j) {
-                    if (!wait_bar(BAR(C::kBarVFull + j % NSV), (j / NSV) & 1, abort_flag))
-                        return false;
-                    v_seen = j;
-                    tc_fence_after();
-                }
-                const uint32_t vb = sV + (j % NSV) * C::kTileBytes;
+            // [O | rowsum] += P(j) [V_j | ones], P read from the TMEM of S buffer j % 2
+            auto issue_pv = [&](int j) -> bool {
+                if (!wait_c(BAR(C::kBarVFull + j % NSV), (j / NSV) & 1, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t vb = sV + (j % NSV) * C::kVStageBytes;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_ts(tmem + C::col_o(qt), tmem + C::col_s(qt) + kk * 8,
-                              make_sdesc(vb + kk * 2048, C::kChunkBytes, 1024), kIdescO,
+                    tc_mma_ts(tmem + C::kColO, tmem + C::col_s(j & 1) + p_col(kk >> 1) + (kk & 1) * 8,
+                              make_sdesc(vb + kk * 2048, kChunkBytes, 1024), kIdescO,
                               (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(BAR(C::kBarODone + qt));
+                tc_commit(BAR(C::kBarODone));
+                tc_commit(BAR(C::kBarVEmpty + j % NSV));
                 return true;
             };
-            // For each key tile j and query tile: wait P(j), PV(j), then S(j+1).
-            // K tile j+1 is released after its S products, V tile j after its PV.
-            for (int qt = 0; qt < 2 && ok; ++qt)
-                if (ntiles[qt] > 0) ok = issue_s(qt, 0);
-            if (ok) tc_commit(BAR(C::kBarKEmpty + 0));
-            for (int j = 0; ok && j < nj; ++j) {
-                for (int qt = 0; qt < 2; ++qt) {
-                    if (j >= ntiles[qt]) continue;
-                    if (!(ok = wait_bar(BAR(C::kBarPFull + qt), j & 1, abort_flag))) break;
-                    tc_fence_after();
-                    if (!(ok = issue_pv(qt, j))) break;
-                    if (j + 1 < ntiles[qt]) {
-                        // S(j+1) overwrites the TMEM that PV(j) reads as P; both
-                        // are tcgen05.mma issued in order by this thread.
-                        if (kWaitPvBeforeS) {
-                            if (!(ok = wait_bar(BAR(C::kBarODone + qt), j & 1, abort_flag))) break;
-                            tc_fence_after();
-                        }
-                        if (!(ok = issue_s(qt, j + 1))) break;
-                    }
-                }
-                if (!ok) break;
-                tc_commit(BAR(C::kBarVEmpty + j % NSV));
-                if (j + 1 < nj) tc_commit(BAR(C::kBarKEmpty + (j + 1) % NSK));
+            // S runs two tiles ahead of PV: while the softmax works on S(j+1),
+            // the tensor core computes PV(j) and S(j+2).
+            if (ok) ok = issue_s(0);
+            if (ok && n > 1) ok = issue_s(1);
+            for (int j = 0; ok && j < n; ++j) {
+                if (!(ok = wait_c(BAR(C::kBarPFull), j & 1, abort_flag))) break;
+                tc_fence_after();
+                if (!(ok = issue_pv(j))) break;
+                // S(j+2) overwrites the TMEM that PV(j) reads as P; both are
+                // tcgen05.mma issued in order by this thread.
+                if (j + 2 < n && !(ok = issue_s(j + 2))) break;
             }
             // every MMA this thread issued completes before the block exits
             tc_commit(BAR(C::kBarDrain));
-            wait_bar_drain(BAR(C::kBarDrain), 0);
+            wait_bar_drain(BAR(C::kBarDrain), 0, &g_tc_status);
         }
         __syncwarp();
+      }
     } else {
         // ------------------------------------------------------ softmax
-        const int qt = warp >> 2, wq = warp & 3;
-        const int n = ntiles[qt];
+        const int half = warp >> 2, wq = warp & 3;
         const int irow = wq * 32 + lane;
-        const int r = row0[qt] + irow;
+        const int r = row0 + irow;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const uint32_t tS = tmem + lane_off + C::col_s(qt);
-        const uint32_t tO = tmem + lane_off + C::col_o(qt);
+        const uint32_t tO = tmem + lane_off + C::kColO;
+        float *xmax = reinterpret_cast<float *>(smem + C::kOffXMax);
+        float *xcarry = reinterpret_cast<float *>(smem + C::kOffXCarry);
+        float *xfin = reinterpret_cast<float *>(smem + C::kOffXFin);
+        const uint32_t xbar = BAR(C::kBarX);
+        uint32_t xe = 0;  // exchanges completed on xbar
         RowState st;
         st.k2 = p.k2;
         st.m_run = -INFINITY;
-        st.l_run = st.l_bf = st.carry = st.w_sink = st.s_sink = 0.0f;
-        bool ok = n > 0;
-        if (CONT && ok && p.mode == 2) {
-            ok = __all_sync(0xffffffffu, wait_bar(BAR(C::kBarQ), 0, abort_flag));
+        st.l_run = st.w_sink = st.s_sink = 0.0f;
+        bool ok = true;
+        if (half == 0 && p.mode == 2) {
+            ok = __all_sync(0xffffffffu, wait_c(BAR(C::kBarQ), 0, abort_flag));
             if (ok) {
                 // s_sink = q_r . k0[h], from this row of the swizzled Q tile
                 const __nv_bfloat16 *k0h = p.k0 + (size_t)(bh % p.H) * D;
@@ -587,8 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < C::kChunks; ++cc) {
 #pragma unroll
                     for (int kc = 0; kc < 8; ++kc) {
-                        const uint8_t *src = smem + C::kOffQ + qt * C::kTileBytes +
-                                             cc * C::kChunkBytes + irow * 128 +
+                        const uint8_t *src = smem + C::kOffQ + cc * kChunkBytes + irow * 128 +
                                              ((kc ^ (irow & 7)) << 4);
                         const uint4 qv = *reinterpret_cast<const uint4 *>(src);
                         const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(&qv);
@@ -602,62 +487,121 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         for (int j = 0; ok && j < n; ++j) {
-            ok = __all_sync(0xffffffffu, wait_bar(BAR(C::kBarSFull + qt), j & 1, abort_flag));
+            const uint32_t tS = tmem + lane_off + C::col_s(j & 1);
+            ok = __all_sync(0xffffffffu,
+                            wait_c(BAR(C::kBarSFull + (j & 1)), (j >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
             // last valid column of this row, and whether the tile needs masks
-            const int c_last = CONT ? r + 1 - 127 * j : r - 128 * j;
-            const bool masked = CONT ? (127 * j + 127 > row0[qt] + 1) : (128 * j + 127 > row0[qt]);
-            const int sink = (CONT && j == 0) ? p.mode : 0;
-            float alpha;
-            bool grow;
+            const int c_last = r + 1 - 127 * j;
+            const bool masked = 127 * j + 127 > row0 + 1;
+            const int sink = j == 0 ? p.mode : 0;
+            // this half's 64 logits and its neighbour column (64 or 63)
+            uint32_t a[2][32];
+            uint32_t nb[1] = {0u};
+            tmem_ld32(tS + 64 * half, a[0]);
+            tmem_ld32(tS + 64 * half + 32, a[1]);
+            tmem_ld1(tS + (half == 0 ? 64 : 63), nb[0]);
+            tmem_wait_ld_regs<32>(a[0]);
+            tmem_wait_ld_regs<32>(a[1]);
+            tmem_wait_ld_regs<1>(nb);
+            float s0 = __uint_as_float(a[0][0]);
+            if (half == 0 && sink == 1) s0 = __uint_as_float(a[0][1]);
+            if (half == 0 && sink == 2) s0 = st.s_sink;
+            const float mine = masked ? half_max<true>(a, half, c_last, s0)
+                                      : half_max<false>(a, half, c_last, s0);
+            // exchange the partial maxima (and the carried L share) with the other half
+            const int slot = xe & 1;
+            xmax[(slot * 2 + half) * 128 + irow] = mine;
+            mbar_arrive(xbar);
+            ok = __all_sync(0xffffffffu, wait_c(xbar, xe & 1, abort_flag));
+            ++xe;
+            if (!ok) break;
+            const float mx = fmaxf(mine, xmax[(slot * 2 + (half ^ 1)) * 128 + irow]);
+            float Lc = 0.0f;
+            if (half == 0 && j > 0) Lc = xcarry[slot * 128 + irow];
+            const float mt = (!masked || c_last >= 0) ? mx * st.k2 : -INFINITY;
+            float alpha = 1.0f;
+            const bool grow = mt > st.m_run + 8.0f;
+            if (grow) {
+                alpha = ex2_approx(st.m_run - mt);
+                st.m_run = mt;
+                st.l_run *= alpha;
+                st.w_sink *= alpha;
+                Lc *= alpha;
+            }
+            const float nm = -st.m_run;
             if (masked)
-                grow = softmax_tile<CONT, true>(tS, st, c_last, sink, alpha);
+                half_weights<true>(tS, a, nb[0], st, half, c_last, sink, nm, Lc);
             else
-                grow = softmax_tile<CONT, false>(tS, st, c_last, sink, alpha);
-            // Rescale O when this row's max moved (after PV(j-1) finished).
+                half_weights<false>(tS, a, nb[0], st, half, c_last, sink, nm, Lc);
+            if (half == 1) xcarry[(xe & 1) * 128 + irow] = Lc;
+            // Rescale O (this half's value columns; half 1 also the row-sum
+            // column) when the max moved, after PV(j-1) finished.
             const bool need_o = grow && j > 0;
             if (__any_sync(0xffffffffu, need_o)) {
-                ok = __all_sync(0xffffffffu,
-                                wait_bar(BAR(C::kBarODone + qt), (j - 1) & 1, abort_flag));
+                ok = __all_sync(0xffffffffu, wait_c(BAR(C::kBarODone), (j - 1) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
-                const float a = need_o ? alpha : 1.0f;
+                const float s = need_o ? alpha : 1.0f;
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
+                for (int cc = 0; cc < D / 64; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(tO + 32 * cc, o);
-                    tmem_wait_ld();
+                    const uint32_t ta = tO + half * (D / 2) + 32 * cc;
+                    tmem_ld32(ta, o);
+                    tmem_wait_ld_regs<32>(o);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
-                    tmem_st32(tO + 32 * cc, o);
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * s);
+                    tmem_st32(ta, o);
+                }
+                if (half == 1) {
+                    uint32_t o[1];
+                    tmem_ld1(tO + D, o[0]);
+                    tmem_wait_ld_regs<1>(o);
+                    o[0] = __float_as_uint(__uint_as_float(o[0]) * s);
+                    tmem_st1(tO + D, o[0]);
                 }
                 tmem_wait_st();
             }
             tc_fence_before();
-            mbar_arrive(BAR(C::kBarPFull + qt));
+            mbar_arrive(BAR(C::kBarPFull));
         }
-        if (ok && n > 0) {
-            ok = __all_sync(0xffffffffu, wait_bar(BAR(C::kBarODone + qt), (n - 1) & 1, abort_flag));
+        if (ok) {
+            // combine the two halves' fp32 sums; the given sink's weight lives in half 0
+            float *mine = xfin + (half * 128 + irow) * 2;
+            mine[0] = st.l_run;
+            mine[1] = st.w_sink;
+            mbar_arrive(xbar);
+            ok = __all_sync(0xffffffffu, wait_c(xbar, xe & 1, abort_flag));
+            ++xe;
+        }
+        if (ok) {
+            const float *oth = xfin + ((half ^ 1) * 128 + irow) * 2;
+            const float l_run = st.l_run + oth[0];
+            const float w_sink = half == 0 ? st.w_sink : oth[1];
+            ok = __all_sync(0xffffffffu, wait_c(BAR(C::kBarODone), (n - 1) & 1, abort_flag));
             if (ok) {
                 tc_fence_after();
-                // the continuous kernel divides by the bf16-rounded weight sum that
-                // fed the PV product; the standard one by the fp32 sum
-                const float inv_l = 1.0f / (CONT ? st.l_bf : st.l_run);
+                // o is divided by the sum of exactly the bf16 weights that fed the
+                // PV product (O column d) plus the given sink's fp32 weight
+                uint32_t lb[1];
+                tmem_ld1(tO + D, lb[0]);
+                tmem_wait_ld_regs<1>(lb);
+                const float inv_l = 1.0f / (__uint_as_float(lb[0]) + w_sink);
                 const bool store = r < T;
-                __nv_bfloat16 *orow = p.out + ((size_t)bh * T + (size_t)(store ? r : 0)) * D;
-                const __nv_bfloat16 *v0h = p.v0 + (size_t)(bh % p.H) * D;
+                __nv_bfloat16 *orow =
+                    p.out + ((size_t)bh * T + (size_t)(store ? r : 0)) * D + half * (D / 2);
+                const __nv_bfloat16 *v0h = p.v0 + (size_t)(bh % p.H) * D + half * (D / 2);
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
+                for (int cc = 0; cc < D / 64; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(tO + 32 * cc, o);
-                    tmem_wait_ld();
+                    tmem_ld32(tO + half * (D / 2) + 32 * cc, o);
+                    tmem_wait_ld_regs<32>(o);
                     float val[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         float x = __uint_as_float(o[e]);
-                        if (CONT && p.mode == 2)
-                            x = fmaf(st.w_sink, __bfloat162float(v0h[32 * cc + e]), x);
+                        if (p.mode == 2) x = fmaf(w_sink, __bfloat162float(v0h[32 * cc + e]), x);
                         val[e] = x * inv_l;
                     }
                     uint32_t pk[16];
@@ -670,9 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                     }
                 }
-                if (store && p.lse)
-                    p.lse[(size_t)bh * T + r] =
-                        (st.m_run + log2f(st.l_run)) * kLn2 + (CONT ? kLseShift : 0.0f);
+                if (store && half == 0 && p.lse)
+                    p.lse[(size_t)bh * T + r] = (st.m_run + log2f(l_run)) * kLn2 + kLseShift;
             }
         }
     }
@@ -680,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 9) tmem_dealloc(tmem, 512);
+    if (warp == kWarpMma) tmem_dealloc(tmem, 512);
 #undef BAR
 }
 
@@ -714,36 +657,7 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns) {
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// [B*H, T, D] bf16 viewed as a 3-D tensor, boxes of 64 columns x 128 rows.
-bool encode_qkv_map(CUtensorMap *map, const void *ptr, int BH, int T, int D) {
-    auto fn = get_encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)BH};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult rc = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
-                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return rc == CUDA_SUCCESS;
-}
-
-template <int D, bool CONT>
+template <int D>
 int launch_tc(const void *q, const void *k, const void *v, const void *k0, const void *v0,
               void *out, float *lse, int B, int H, int T, float scale, int mode,
               cudaStream_t stream) {
@@ -757,16 +671,16 @@ int launch_tc(const void *q, const void *k, const void *v, const void *k0, const
     prm.B = B;
     prm.H = H;
     prm.T = T;
-    prm.num_pairs = (T + 255) / 256;
+    prm.num_qtiles = (T + 127) / 128;
     prm.k2 = scale * kLog2e;
     prm.mode = mode;
     prm.k0 = static_cast<const __nv_bfloat16 *>(k0);
     prm.v0 = static_cast<const __nv_bfloat16 *>(v0);
     prm.out = static_cast<__nv_bfloat16 *>(out);
     prm.lse = lse;
-    const long long grid = (long long)prm.num_pairs * BH;
+    const long long grid = (long long)prm.num_qtiles * BH;
     if (grid > 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
-    auto kern = tc_forward_kernel<D, CONT>;
+    auto kern = tc_forward_kernel<D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return CSA_ERR_CUDA;
@@ -778,13 +692,9 @@ int launch_tc(const void *q, const void *k, const void *v, const void *k0, const
 
 int csa_tc_forward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
                    void *out, float *lse, int B, int H, int T, int d, float scale, int mode,
-                   bool continuous, cudaStream_t stream) {
-    if (d == 128)
-        return continuous ? launch_tc<128, true>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream)
-                          : launch_tc<128, false>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
-    if (d == 64)
-        return continuous ? launch_tc<64, true>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream)
-                          : launch_tc<64, false>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
+                   cudaStream_t stream) {
+    if (d == 128) return launch_tc<128>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
+    if (d == 64) return launch_tc<64>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
     return CSA_ERR_UNSUPPORTED;
 }
 
