@@ -54,6 +54,39 @@ def _dist_env():
     return ws, rank, local
 
 
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "csa_forward_headline.md")
+KERNEL_SOURCES = ["csa_tc.cu", "csa_tc_common.cuh", "csa_device.cuh"]
+
+
+def kernel_source_hash():
+    """sha256 over the sources of the continuous tensor-core kernel."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "continuous_softmax_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the headline kernel from the committed ncu
+    summary, or None when the kernel sources changed since it was taken."""
+    try:
+        fields = {}
+        with open(PROFILE_SUMMARY) as f:
+            for line in f:
+                line = line.strip().strip("`")
+                for key in ("traffic_bytes_per_launch:", "source_sha256:"):
+                    if line.startswith(key):
+                        fields[key] = line[len(key):].strip()
+        if fields.get("source_sha256:") != kernel_source_hash():
+            return None
+        return int(fields["traffic_bytes_per_launch:"])
+    except Exception:
+        return None
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -245,7 +278,9 @@ def run_gpu(args):
         "gpu_launches": K,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": burst,
                      "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
-                     "peak_source": f"{src} bf16 dense (burst)", "traffic": None},
+                     "peak_source": f"{src} bf16 dense (burst)", "traffic": recorded_traffic(),
+                     "traffic_unit": "bytes per launch (ncu dram read+write)",
+                     "algorithmic_bytes": 2 * 4 * B * H * T * d + 4 * B * H * T},
         "clocks": clocks,
         "device_status": status,
         "wall_s": round(t_wall, 3),

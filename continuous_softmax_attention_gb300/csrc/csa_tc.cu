@@ -108,6 +108,7 @@ struct TcCfg {
 struct TcParams {
     int B, H, T;
     int num_qtiles;
+    int group;  // heads per scheduling group
     float k2;  // scale * log2(e)
     int mode;
     const __nv_bfloat16 *k0;
@@ -306,9 +307,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int BH = p.B * p.H;
-    const int bh = (int)(blockIdx.x % (unsigned)BH);
-    const int qtile = p.num_qtiles - 1 - (int)(blockIdx.x / (unsigned)BH);
+    // Heads go in groups whose K/V fit in L2 together; within a group the
+    // heaviest query tiles go first (longest-first keeps the tail short).
+    const int nq = p.num_qtiles, BH = p.B * p.H;
+    const int grp = (int)(blockIdx.x / (unsigned)(p.group * nq));
+    const int gsz = min(p.group, BH - grp * p.group);
+    const int idx = (int)blockIdx.x - grp * p.group * nq;
+    const int bh = grp * p.group + idx % gsz;
+    const int qtile = nq - 1 - idx / gsz;
     const int T = p.T;
     const int row0 = qtile * 128;
     const int n = (min(row0 + 127, T - 1) + 1) / 127 + 1;  // key tiles of this query tile
@@ -672,6 +678,7 @@ int launch_tc(const void *q, const void *k, const void *v, const void *k0, const
     prm.H = H;
     prm.T = T;
     prm.num_qtiles = (T + 127) / 128;
+    prm.group = heads_per_group(BH, T, D);
     prm.k2 = scale * kLog2e;
     prm.mode = mode;
     prm.k0 = static_cast<const __nv_bfloat16 *>(k0);

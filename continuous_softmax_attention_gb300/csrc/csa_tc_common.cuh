@@ -91,6 +91,16 @@ __device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity, in
 }
 
 // ---------------------------------------------------------------- host side
+// Heads per scheduling group: as many as keep the group's K and V (bf16)
+// within 64 MiB, half of L2, so that they are read from HBM about once.
+inline int heads_per_group(int BH, int T, int D) {
+    const long long per_head = 2LL * T * D * 2;
+    long long g = (64LL << 20) / (per_head > 0 ? per_head : 1);
+    if (g < 1) g = 1;
+    if (g > BH) g = BH;
+    return (int)g;
+}
+
 inline PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;

@@ -67,6 +67,7 @@ struct StdCfg {
 struct StdParams {
     int B, H, T;
     int num_pairs;
+    int group;  // heads per scheduling group
     float k2;  // scale * log2(e)
     __nv_bfloat16 *out;
     float *lse;
@@ -165,9 +166,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int BH = p.B * p.H;
-    const int bh = (int)(blockIdx.x % (unsigned)BH);
-    const int pair = p.num_pairs - 1 - (int)(blockIdx.x / (unsigned)BH);
+    // Heads go in groups whose K/V fit in L2 together; within a group the
+    // heaviest query tiles go first (longest-first keeps the tail short).
+    const int nq = p.num_pairs, BH = p.B * p.H;
+    const int grp = (int)(blockIdx.x / (unsigned)(p.group * nq));
+    const int gsz = min(p.group, BH - grp * p.group);
+    const int idx = (int)blockIdx.x - grp * p.group * nq;
+    const int bh = grp * p.group + idx % gsz;
+    const int pair = nq - 1 - idx / gsz;
     const int T = p.T;
     int row0[2], ntiles[2];
 #pragma unroll
@@ -395,6 +401,7 @@ int launch_std(const void *q, const void *k, const void *v, void *out, float *ls
     prm.H = H;
     prm.T = T;
     prm.num_pairs = (T + 255) / 256;
+    prm.group = heads_per_group(BH, T, D);
     prm.k2 = scale * kLog2e;
     prm.out = static_cast<__nv_bfloat16 *>(out);
     prm.lse = lse;
