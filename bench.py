@@ -160,6 +160,7 @@ def run_gpu(args):
     import torch.distributed as dist
 
     import continuous_softmax_attention_gb300 as csa
+    from continuous_softmax_attention_gb300.dist import max_over_ranks
     from continuous_softmax_attention_gb300.inputs import WORKLOADS, algorithmic_flops, workload_inputs
 
     ws, rank, local = _dist_env()
@@ -235,10 +236,7 @@ def run_gpu(args):
     status = csa.device_status()
 
     def total(ms):
-        t = torch.tensor([sum(ms)], dtype=torch.float64, device=dev)
-        if ws > 1:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return t.item()
+        return max_over_ranks(sum(ms), device=dev)
 
     tot_csa, tot_std, tot_e2e = total(ms_csa), total(ms_std), total(ms_e2e)
     if ws > 1:

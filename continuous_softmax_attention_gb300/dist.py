@@ -1,0 +1,84 @@
+"""Multi-GPU use of the forward pass: one process per GPU, no collective on
+the data path.
+
+The (b, h) problems of a batch are independent (each head's rows attend
+only its own keys), so N ranks split the B*H problems into contiguous
+shards, each runs the CUDA kernel on its shard, and an all-gather assembles
+the result where the caller wants it in one place.  The only collectives are
+that optional gather, a barrier and the max of timings in the benchmark.
+"""
+from __future__ import annotations
+
+import torch
+import torch.distributed as dist
+
+
+def head_shard(n_problems: int, world: int, rank: int):
+    """Contiguous, balanced [start, stop) of the flattened (b, h) problems."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("bad world/rank")
+    base, extra = divmod(n_problems, world)
+    start = rank * base + min(rank, extra)
+    stop = start + base + (1 if rank < extra else 0)
+    return start, stop
+
+
+def shard_inputs(q, k, v, k0, v0, world: int, rank: int):
+    """This rank's problems as a [1, n, T, d] batch (views of q, k, v) and,
+    for the per-head sink pair, the matching [n, d] rows of k0 and v0."""
+    B, H, T, d = q.shape
+    start, stop = head_shard(B * H, world, rank)
+    flat = lambda t: t.reshape(B * H, T, d)[start:stop].unsqueeze(0)
+    heads = torch.arange(start, stop, device=q.device) % H
+    k0s = k0.index_select(0, heads) if k0 is not None else None
+    v0s = v0.index_select(0, heads) if v0 is not None else None
+    return flat(q), flat(k), flat(v), k0s, v0s, (start, stop)
+
+
+def gather_outputs(o_s, lse_s, B: int, H: int, world: int, group=None):
+    """All-gather of the shards of every rank into full [B, H, T, d] and
+    [B, H, T] tensors (shards padded to the largest size for the exchange)."""
+    _, n, T, d = o_s.shape
+    sizes = [head_shard(B * H, world, r) for r in range(world)]
+    width = max(b - a for a, b in sizes)
+    pad_o = torch.zeros((width, T, d), dtype=o_s.dtype, device=o_s.device)
+    pad_l = torch.zeros((width, T), dtype=lse_s.dtype, device=lse_s.device)
+    pad_o[:n] = o_s[0]
+    pad_l[:n] = lse_s[0]
+    go = [torch.empty_like(pad_o) for _ in range(world)]
+    gl = [torch.empty_like(pad_l) for _ in range(world)]
+    dist.all_gather(go, pad_o, group=group)
+    dist.all_gather(gl, pad_l, group=group)
+    o = torch.cat([go[r][: b - a] for r, (a, b) in enumerate(sizes)]).reshape(B, H, T, d)
+    lse = torch.cat([gl[r][: b - a] for r, (a, b) in enumerate(sizes)]).reshape(B, H, T)
+    return o, lse
+
+
+def forward_sharded(q, k, v, k0=None, v0=None, *, mode: int = 0, scale=None, gather=True,
+                    group=None, fn=None):
+    """Runs the forward pass on this rank's share of the (b, h) problems.
+
+    fn(q, k, v, k0, v0, mode=, scale=) -> (o, lse) computes one shard; it is
+    the CUDA kernel (continuous_softmax_attention_gb300.forward) by default.
+    Returns the full (o, lse) when gather is true, else this rank's shard and
+    its [start, stop) range."""
+    world = dist.get_world_size(group) if dist.is_initialized() else 1
+    rank = dist.get_rank(group) if dist.is_initialized() else 0
+    if fn is None:
+        from . import forward as fn
+    qs, ks, vs, k0s, v0s, rng = shard_inputs(q, k, v, k0, v0, world, rank)
+    o_s, lse_s = fn(qs.contiguous(), ks.contiguous(), vs.contiguous(), k0s, v0s, mode=mode,
+                    scale=scale)
+    if not gather or world == 1:
+        return (o_s, lse_s) if gather else (o_s, lse_s, rng)
+    B, H = q.shape[0], q.shape[1]
+    return gather_outputs(o_s, lse_s, B, H, world, group)
+
+
+def max_over_ranks(value: float, device=None, group=None) -> float:
+    """The largest value over all ranks (the benchmark's timed region)."""
+    if not dist.is_initialized() or dist.get_world_size(group) == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
