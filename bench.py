@@ -19,6 +19,12 @@ Also reported on the same JSON line:
                bounded sample of rows of the same workload
   clocks       nvidia-smi SM clocks and throttle reasons sampled during the
                timed region
+  decode       the decode step (csa_decode: the newest token of 16 sequences
+               of lengths in [4096, 8192] against their KV cache, H=32,
+               d=128), an HBM-bound path: cache bytes read / call time
+               against the measured copy bandwidth, plus its own e2e (the
+               queries from pinned host memory, outputs back to the host;
+               the cache stays resident as it would while serving)
 
 `--impl reference` times the CPU oracle alone (the reference arm).
 Multi-GPU (torchrun): every rank runs its own copy of the workload (the
@@ -201,6 +207,8 @@ def run_gpu(args):
     csa_call = lambda: csa.forward(g["q"], g["k"], g["v"], mode=w.modes[0], scale=scale, out=out, lse=lse)
     std_call = lambda: csa.std_forward(g["q"], g["k"], g["v"], scale=scale, out=out, lse=lse)
 
+    dec = None if args.no_decode else DecodeBench(csa, dev, stream, flush)
+
     # end to end through the C ABI with host buffers
     pin = {k: x[k].pin_memory() for k in ("q", "k", "v")}
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -222,6 +230,9 @@ def run_gpu(args):
         csa_call()
         std_call()
         e2e_call()
+        if dec is not None:
+            dec.call()
+            dec.e2e_call()
     torch.cuda.synchronize()
     assert csa.device_status() == 0
 
@@ -231,6 +242,9 @@ def run_gpu(args):
         ms_csa = timed(csa_call, args.steps)
         ms_std = timed(std_call, args.steps)
         ms_e2e = timed(e2e_call, args.steps)
+        if dec is not None:
+            dec.ms = timed(dec.call, args.decode_steps)
+            dec.ms_e2e = timed(dec.e2e_call, args.decode_steps)
     barrier()
     t_wall = time.perf_counter() - t_wall
     status = csa.device_status()
@@ -273,7 +287,7 @@ def run_gpu(args):
                 "ratio_continuous_over_std": round(value / std_value, 4)},
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "ms_per_step": round(tot_e2e / K, 5),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": K,
+        "gpu_launches": 3 * K + (0 if dec is None else 2 * 2 * args.decode_steps),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": burst,
                      "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
                      "peak_source": f"{src} bf16 dense (burst)", "traffic": recorded_traffic(),
@@ -283,9 +297,84 @@ def run_gpu(args):
         "device_status": status,
         "wall_s": round(t_wall, 3),
     }
+    if dec is not None:
+        line["decode"] = dec.summary(ws, args.decode_steps, max_over_ranks, dev)
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = cpu_baseline(x, scale, budget_s=args.cpu_seconds)
     return line
+
+
+class DecodeBench:
+    """The decode workload: resident cache, one csa_decode call per step."""
+
+    def __init__(self, csa, dev, stream, flush):
+        import torch
+
+        from continuous_softmax_attention_gb300.inputs import (DECODE_WORKLOADS, decode_bytes,
+                                                               decode_workload_inputs)
+
+        self.w = w = DECODE_WORKLOADS["decode"]
+        x = decode_workload_inputs("decode")
+        self.lens = x["seqlens"].tolist()
+        self.bytes = decode_bytes(self.lens, w.H, w.d)
+        g = {k: t.to(dev) for k, t in x.items()}
+        self.q, self.k, self.v, self.sl = g["q"], g["k"], g["v"], g["seqlens"]
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(csa.decode_workspace_bytes(w.B, w.H, w.T, w.d), dtype=torch.uint8,
+                              device=dev)
+        self.pin_q = x["q"].pin_memory()
+        self.dq = torch.empty_like(self.q)
+        self.host_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.host_lse = torch.empty(self.lse.shape, dtype=self.lse.dtype).pin_memory()
+        self.csa = csa
+        self.ms = self.ms_e2e = None
+
+    def call(self):
+        self.csa.decode(self.q, self.k, self.v, seqlens=self.sl, mode=self.w.mode, out=self.out,
+                        lse=self.lse, workspace=self.ws)
+
+    def e2e_call(self):
+        self.dq.copy_(self.pin_q, non_blocking=True)
+        self.csa.decode(self.dq, self.k, self.v, seqlens=self.sl, mode=self.w.mode, out=self.out,
+                        lse=self.lse, workspace=self.ws)
+        self.host_out.copy_(self.out, non_blocking=True)
+        self.host_lse.copy_(self.lse, non_blocking=True)
+
+    def summary(self, world, steps, max_over_ranks, dev):
+        w = self.w
+        tot = max_over_ranks(sum(self.ms), device=dev)
+        tot_e2e = max_over_ranks(sum(self.ms_e2e), device=dev)
+        ms = tot / steps
+        gbs = world * self.bytes * steps / (tot * 1e-3) / 1e9
+        gbs_e2e = world * self.bytes * steps / (tot_e2e * 1e-3) / 1e9
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                peak, src = float(json.load(f)["hbm_gbs"]), "measured"
+        except Exception:
+            peak, src = 6800.0, "fallback"
+        achieved = self.bytes / (ms * 1e-3) / 1e9
+        h2d = self.pin_q.numel() * self.pin_q.element_size()
+        d2h = (self.host_out.numel() * self.host_out.element_size() +
+               self.host_lse.numel() * self.host_lse.element_size())
+        return {
+            "metric": f"continuous-attn decode step HBM GB/s (B={w.B},H={w.H},T<={w.T},d={w.d}, bf16)",
+            "value": round(gbs, 2), "unit": "GB/s", "ms_per_step": round(ms, 5), "steps": steps,
+            "tokens_per_s": round(world * w.B * steps / (tot * 1e-3), 1),
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "T_capacity": w.T, "d": w.d,
+                       "lengths": f"uniform in [{w.len_lo}, {w.T}], total {sum(self.lens)}",
+                       "k0_mode": "zero", "l2": "512 MiB flush before every step; cache "
+                       f"{2 * sum(self.lens) * w.H * w.d * 2 / 2**30:.2f} GiB > L2"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_source": f"{src} copy bandwidth", "traffic": None,
+                         "algorithmic_bytes": self.bytes,
+                         "timed": "whole csa_decode call (chunk kernel + merge kernel)"},
+            "e2e": {"value": round(gbs_e2e, 2), "unit": "GB/s", "ms_per_step": round(tot_e2e / steps, 5),
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "note": "queries copied in and outputs copied out each step; cache resident"},
+            "gpu_launches_per_step": 2,
+        }
 
 
 def _sample_rows(T, H, nrows, seed=0):
@@ -382,6 +471,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=256, help="oracle rows per reference step")
+    ap.add_argument("--decode-steps", type=int, default=200, help="timed steps of the decode workload")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

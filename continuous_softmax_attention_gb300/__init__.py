@@ -8,6 +8,8 @@ loudly when the library has not been built.
 from .inputs import ZERO, COPY_FIRST, GIVEN  # noqa: F401
 from ._lib import (  # noqa: F401
     CsaError,
+    decode,
+    decode_workspace_bytes,
     device_status,
     forward,
     logphi2_eval,
@@ -18,6 +20,7 @@ from ._lib import (  # noqa: F401
 )
 
 __all__ = [
-    "ZERO", "COPY_FIRST", "GIVEN", "CsaError", "forward", "std_forward", "logphi2_eval",
+    "ZERO", "COPY_FIRST", "GIVEN", "CsaError", "forward", "std_forward", "decode",
+    "decode_workspace_bytes", "logphi2_eval",
     "segment_weights_eval", "device_status", "selftest_wait_timeout", "status_string",
 ]

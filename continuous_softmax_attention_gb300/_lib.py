@@ -53,10 +53,14 @@ def load():
                        ("csa_segment_weights_eval", [p, p, p, p, i, p]),
                        ("csa_device_status", []),
                        ("csa_selftest_wait_timeout", [u, p]),
-                       ("csa_abi_version", [])):
+                       ("csa_abi_version", []),
+                       ("csa_decode", [p, p, p, p, p, p, p, p, p, ctypes.c_longlong, i, i, i, i,
+                                       f, i, p])):
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = i
+    lib.csa_decode_workspace_bytes.argtypes = [i, i, i, i]
+    lib.csa_decode_workspace_bytes.restype = ctypes.c_longlong
     lib.csa_status_string.argtypes = [i]
     lib.csa_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -174,6 +178,61 @@ def std_forward(q, k, v, *, scale=None, out=None, lse=None, stream=None, want_ls
         raise ValueError(f"unsupported dtype {dtype}")
     _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, T, d, float(scale),
               _stream_handle(stream)), where)
+    return out, lse
+
+
+def decode_workspace_bytes(B: int, H: int, T: int, d: int) -> int:
+    """Bytes of workspace csa_decode needs (host-side, no device needed)."""
+    n = int(load().csa_decode_workspace_bytes(int(B), int(H), int(T), int(d)))
+    if n < 0:
+        raise CsaError(CSA_ERR_UNSUPPORTED, "csa_decode_workspace_bytes")
+    return n
+
+
+def decode(q, k_cache, v_cache, k0=None, v0=None, *, seqlens=None, mode: int = 0, scale=None,
+           out=None, lse=None, workspace=None, stream=None, want_lse: bool = True):
+    """One decode step: the newest token of each sequence against its cache.
+
+    q: bf16 CUDA [B, H, d]; k_cache, v_cache: bf16 [B, H, T, d]; seqlens: int32
+    CUDA [B] with the used lengths n_b (None: all T).  k0, v0: [H, d] in mode
+    GIVEN (2).  workspace: a uint8 CUDA tensor of at least
+    decode_workspace_bytes(B, H, T, d) bytes (allocated when None).
+    Returns (o [B, H, d], lse [B, H])."""
+    import torch
+
+    B, H, T, d = k_cache.shape
+    dev = k_cache.device
+    bf = torch.bfloat16
+    _check_tensor(k_cache, "k_cache", bf, (B, H, T, d), dev)
+    _check_tensor(v_cache, "v_cache", bf, (B, H, T, d), dev)
+    _check_tensor(q, "q", bf, (B, H, d), dev)
+    if mode == 2:
+        if k0 is None or v0 is None:
+            raise ValueError("mode 2 (given sink) needs k0 and v0")
+        _check_tensor(k0, "k0", bf, (H, d), dev)
+        _check_tensor(v0, "v0", bf, (H, d), dev)
+    else:
+        k0 = v0 = None
+    if seqlens is not None:
+        _check_tensor(seqlens, "seqlens", torch.int32, (B,), dev)
+    if scale is None:
+        scale = 1.0 / d ** 0.5
+    if out is None:
+        out = torch.empty((B, H, d), dtype=bf, device=dev)
+    _check_tensor(out, "out", bf, (B, H, d), dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _check_tensor(lse, "lse", torch.float32, (B, H), dev)
+    if workspace is None:
+        workspace = torch.empty(max(decode_workspace_bytes(B, H, T, d), 16), dtype=torch.uint8,
+                                device=dev)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on the cache's device")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().csa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k0), _ptr(v0),
+                             _ptr(seqlens), _ptr(out), _ptr(lse), _ptr(workspace), nbytes, B, H,
+                             T, d, float(scale), int(mode), _stream_handle(stream)), "csa_decode")
     return out, lse
 
 

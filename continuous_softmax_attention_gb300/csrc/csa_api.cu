@@ -85,9 +85,47 @@ int forward_f32(const float *q, const float *k, const float *v, const float *k0,
                                           continuous, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int decode_bf16(const void *q, const void *k_cache, const void *v_cache, const void *k0,
+                const void *v0, const int *seqlens, void *out, float *lse, void *workspace,
+                long long workspace_bytes, int B, int H, int T, int d, float scale, int mode,
+                csa_stream_t stream) {
+    if (B < 0 || H < 0 || T < 0 || d < 1) return CSA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return CSA_ERR_INVALID_ARG;
+    if (mode < CSA_K0_ZERO || mode > CSA_K0_GIVEN) return CSA_ERR_INVALID_ARG;
+    if (!(d == 64 || d == 128 || d == 256)) return CSA_ERR_UNSUPPORTED;
+    if ((long long)B * H == 0) return CSA_OK;
+    if (T == 0) return CSA_ERR_INVALID_ARG;  // the newest token's own key is in the cache
+    if (!q || !k_cache || !v_cache || !out || !workspace) return CSA_ERR_INVALID_ARG;
+    if (mode == CSA_K0_GIVEN && (!k0 || !v0)) return CSA_ERR_INVALID_ARG;
+    if ((long long)B * H * T > (1LL << 40)) return CSA_ERR_UNSUPPORTED;
+    const long long need = csa_decode_scratch_bytes(B, H, T, d);
+    if (need < 0) return CSA_ERR_UNSUPPORTED;
+    if (workspace_bytes < need) return CSA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(workspace, 16) || (lse && !aligned(lse, 4)) || (seqlens && !aligned(seqlens, 4)))
+        return CSA_ERR_ALIGNMENT;
+    if (mode == CSA_K0_GIVEN && (!aligned(k0, 16) || !aligned(v0, 16))) return CSA_ERR_ALIGNMENT;
+    int rc = device_ok();
+    if (rc != CSA_OK) return rc;
+    return csa_decode_run(q, k_cache, v_cache, k0, v0, seqlens, out, lse, workspace, B, H, T, d,
+                          scale, mode, reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 extern "C" {
+
+long long csa_decode_workspace_bytes(int B, int H, int T, int d) {
+    return csa_decode_scratch_bytes(B, H, T, d);
+}
+
+int csa_decode(const void *q, const void *k_cache, const void *v_cache, const void *k0,
+               const void *v0, const int *seqlens, void *out, float *lse, void *workspace,
+               long long workspace_bytes, int B, int H, int T, int d, float scale, int k0_mode,
+               csa_stream_t stream) {
+    return decode_bf16(q, k_cache, v_cache, k0, v0, seqlens, out, lse, workspace,
+                       workspace_bytes, B, H, T, d, scale, k0_mode, stream);
+}
 
 int csa_forward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
                 void *out, float *lse, int B, int H, int T, int d, float scale, int k0_mode,
@@ -138,7 +176,8 @@ int csa_device_status(void) {
     if (rc != CSA_OK) return rc;
     const int a = csa_tc_take_status();
     const int b = csa_tc_std_take_status();
-    return a != CSA_OK ? a : b;
+    const int c = csa_decode_take_status();
+    return a != CSA_OK ? a : b != CSA_OK ? b : c;
 }
 
 int csa_selftest_wait_timeout(unsigned timeout_us, csa_stream_t stream) {

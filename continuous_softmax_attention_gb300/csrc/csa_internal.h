@@ -30,3 +30,12 @@ cudaError_t csa_tc_selftest_wait_timeout(unsigned timeout_us, cudaStream_t strea
 // the current device.
 int csa_tc_take_status(void);
 int csa_tc_std_take_status(void);
+
+// Decode step (csa_decode.cu), bf16, d in {64, 128, 256}.  Scratch holds
+// the per-chunk partials; csa_decode_scratch_bytes gives its size (-1 for an
+// unsupported d or a negative size).
+long long csa_decode_scratch_bytes(int B, int H, int T, int d);
+int csa_decode_run(const void *q, const void *k_cache, const void *v_cache, const void *k0,
+                   const void *v0, const int *seqlens, void *out, float *lse, void *scratch, int B,
+                   int H, int T, int d, float scale, int mode, cudaStream_t stream);
+int csa_decode_take_status(void);

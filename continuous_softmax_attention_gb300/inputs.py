@@ -100,3 +100,60 @@ def algorithmic_flops(B, H, T, d, continuous=True):
     row has t pairs."""
     pairs = B * H * (T * (T + 3) // 2 if continuous else T * (T + 1) // 2)
     return 4 * d * pairs
+
+
+# Decode step: the newest token of each of B sequences against its KV cache.
+# Recipe: a CPU generator seeded with `seed` draws q [B, H, d], k, v
+# [B, H, T, d], k0, v0 [H, d] from N(0, 1) in float32, in that order, then the
+# lengths n_b uniformly from the integers [len_lo, T]; tensors are rounded to
+# bf16.  Rows past n_b of the cache are drawn too (they are never read).
+@dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    B: int
+    H: int
+    T: int
+    d: int
+    seed: int
+    len_lo: int
+    mode: int = ZERO
+    notes: str = ""
+
+
+DECODE_WORKLOADS = {
+    "decode_small": DecodeWorkload("decode_small", 3, 2, 700, 128, 5, 1,
+                                   notes="parity case: several chunks and a ragged tail"),
+    "decode": DecodeWorkload("decode", 16, 32, 8192, 128, 6, 4096,
+                             notes="headline head shape, 16 sequences, lengths in [T/2, T]"),
+}
+
+
+def make_decode_inputs(B, H, T, d, seed=0, len_lo=1):
+    """Returns dict(q, k, v, k0, v0, seqlens) of CPU tensors (bf16, int32)."""
+    if not 1 <= len_lo <= T:
+        raise ValueError("need 1 <= len_lo <= T")
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    bf = lambda *shape: torch.randn(*shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    q = bf(B, H, d)
+    k = torch.empty(B, H, T, d, dtype=torch.bfloat16)
+    v = torch.empty(B, H, T, d, dtype=torch.bfloat16)
+    for t in (k, v):  # one sequence at a time keeps the float32 staging small
+        for b in range(B):
+            t[b] = torch.randn(H, T, d, generator=g, dtype=torch.float32)
+    k0, v0 = bf(H, d), bf(H, d)
+    seqlens = torch.randint(len_lo, T + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+    return {"q": q, "k": k, "v": v, "k0": k0, "v0": v0, "seqlens": seqlens}
+
+
+def decode_workload_inputs(name: str):
+    w = DECODE_WORKLOADS[name]
+    return make_decode_inputs(w.B, w.H, w.T, w.d, w.seed, w.len_lo)
+
+
+def decode_bytes(seqlens, H, d):
+    """HBM bytes a decode step must move: every used cached key and value
+    row once (bf16), the queries and outputs (bf16) and lse (fp32)."""
+    n = int(sum(int(x) for x in seqlens))
+    B = len(seqlens)
+    return 2 * n * H * d * 2 + 2 * B * H * d * 2 + B * H * 4

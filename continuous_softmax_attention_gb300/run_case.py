@@ -1,9 +1,12 @@
-"""Runs the forward kernels a few times at one shape (for profilers).
+"""Runs the kernels a few times at one shape (for profilers).
 
     python -m continuous_softmax_attention_gb300.run_case --B 1 --H 24 --T 8192 --d 128
+    python -m continuous_softmax_attention_gb300.run_case --decode --B 4 --H 32 --T 8192
 
 Inputs come from the seeded generator; each iteration launches the
 continuous kernel once and, unless --no-std, the standard kernel once.
+With --decode each iteration is one decode step (lengths drawn from
+[T/2, T]).
 """
 from __future__ import annotations
 
@@ -25,7 +28,10 @@ def main():
     ap.add_argument("--mode", type=int, default=0)
     ap.add_argument("--iters", type=int, default=2)
     ap.add_argument("--no-std", action="store_true")
+    ap.add_argument("--decode", action="store_true")
     a = ap.parse_args()
+    if a.decode:
+        return run_decode(a)
     x = make_inputs(a.B, a.H, a.T, a.d, "bf16", seed=0)
     g = {k: v.cuda() for k, v in x.items()}
     scale = 1.0 / math.sqrt(a.d)
@@ -33,6 +39,21 @@ def main():
         o, lse = csa.forward(g["q"], g["k"], g["v"], g["k0"], g["v0"], mode=a.mode, scale=scale)
         if not a.no_std:
             csa.std_forward(g["q"], g["k"], g["v"], scale=scale)
+    torch.cuda.synchronize()
+    st = csa.device_status()
+    print(f"ok status={st} o_mean={o.float().abs().mean().item():.5f}")
+    if st != 0:
+        raise SystemExit(1)
+
+
+def run_decode(a):
+    from continuous_softmax_attention_gb300.inputs import make_decode_inputs
+
+    x = make_decode_inputs(a.B, a.H, a.T, a.d, seed=0, len_lo=max(1, a.T // 2))
+    g = {k: v.cuda() for k, v in x.items()}
+    for _ in range(a.iters):
+        o, lse = csa.decode(g["q"], g["k"], g["v"], g["k0"], g["v0"], seqlens=g["seqlens"],
+                            mode=a.mode)
     torch.cuda.synchronize()
     st = csa.device_status()
     print(f"ok status={st} o_mean={o.float().abs().mean().item():.5f}")

@@ -119,6 +119,50 @@ int csa_std_forward_f32(const float *q, const float *k, const float *v, float *o
                         int B, int H, int T, int d, float scale, csa_stream_t stream);
 
 /*
+ * csa_decode - one decode step: for every sequence b and head h, the output
+ *   of the newest token, position t = n_b, against the sink and the n_b
+ *   cached keys and values.
+ *   Defines: eq. (10)/(11) of "Continuous Softmax Attention" ("Assembly and
+ *   Simplification") for the single row t = n_b; the result equals row
+ *   n_b - 1 of csa_forward run on the first n_b tokens, except that the
+ *   weights stay in fp32 (they are not rounded to bf16 for a tensor core).
+ *   q:         bf16 [B, H, d], the newest token's query of each sequence.
+ *   k_cache, v_cache: bf16 [B, H, T, d]; T is the capacity.  Sequence b uses
+ *              rows 0 .. n_b - 1, the last being the newest token's own key
+ *              and value.
+ *   k0, v0:    bf16 [H, d], read in CSA_K0_GIVEN mode only.  In
+ *              CSA_K0_COPY_FIRST the sink is row 0 of the cache.
+ *   seqlens:   DEVICE int32 [B] with n_b, or NULL for n_b = T for every b.
+ *              A length outside [1, T] is not detectable on the host: that
+ *              sequence's out and lse are set to NaN and the sticky status
+ *              word (csa_device_status) records CSA_ERR_INVALID_ARG.
+ *   out:       bf16 [B, H, d]; lse: float [B, H] natural log, or NULL.
+ *   workspace: DEVICE scratch of at least csa_decode_workspace_bytes(B, H,
+ *              T, d) bytes owned by the caller (16-byte aligned); its
+ *              contents on entry do not matter and are overwritten.  Calls
+ *              that run concurrently must use distinct workspaces.
+ *   d must be 64, 128 or 256 (CSA_ERR_UNSUPPORTED otherwise).  q, k_cache,
+ *   v_cache, out, workspace (and k0, v0 in GIVEN mode) must be 16-byte
+ *   aligned.  B * H == 0: CSA_OK, nothing launched.  T == 0 with B * H > 0:
+ *   CSA_ERR_INVALID_ARG (the newest token's key must be in the cache).
+ *   workspace_bytes smaller than needed: CSA_ERR_INVALID_ARG.
+ *   Computed on CUDA cores in fp32 (the step is bound by reading the cache):
+ *   the positions 0..n_b are split into chunks, each chunk's partial sums
+ *   are formed against its own maximum and merged by log-sum-exp.
+ */
+int csa_decode(const void *q, const void *k_cache, const void *v_cache, const void *k0,
+               const void *v0, const int *seqlens, void *out, float *lse, void *workspace,
+               long long workspace_bytes, int B, int H, int T, int d, float scale, int k0_mode,
+               csa_stream_t stream);
+
+/*
+ * csa_decode_workspace_bytes - bytes of workspace csa_decode needs for these
+ *   sizes (host only, no device needed), or -1 for a negative size or a d
+ *   other than 64, 128, 256.
+ */
+long long csa_decode_workspace_bytes(int B, int H, int T, int d);
+
+/*
  * csa_logphi2_eval - y[i] = log phi2(x[i]) with the library's fp32 device
  *   function (phi2 of eq. (6), "Preliminaries").  x, y: device float arrays
  *   of n elements (n >= 0).  A test hook for the numerics of b.
@@ -139,9 +183,10 @@ int csa_segment_weights_eval(const float *u0, const float *u1, float *right, flo
 
 /*
  * csa_device_status - reads and clears the library's sticky device status
- *   word of the current device: CSA_OK, or CSA_ERR_TIMEOUT if a kernel's
+ *   words of the current device: CSA_OK; CSA_ERR_TIMEOUT if a kernel's
  *   bounded wait expired since the last read (that kernel then skipped the
- *   rest of its work and its outputs are undefined).  Synchronises the
+ *   rest of its work and its outputs are undefined); CSA_ERR_INVALID_ARG if
+ *   csa_decode met a sequence length outside [1, T].  Synchronises the
  *   device.  Returns CSA_ERR_CUDA if the read itself fails.
  */
 int csa_device_status(void);

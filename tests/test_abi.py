@@ -92,3 +92,42 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         L.load()
+
+
+def dec(lib, *, q=FAKE, k=FAKE, v=FAKE, k0=NULL, v0=NULL, seqlens=NULL, out=FAKE, lse=NULL,
+        ws=FAKE, ws_bytes=1 << 30, B=2, H=2, T=300, d=128, scale=0.1, mode=0):
+    return lib.csa_decode(q, k, v, k0, v0, seqlens, out, lse, ws, ws_bytes, B, H, T, d, scale,
+                          mode, None)
+
+
+def test_decode_workspace_bytes(lib):
+    # one chunk of C = 16384/d positions per CTA over positions 0..T, each
+    # leaving d partial outputs plus (max, sum): B*H*(T//C + 1)*(d + 2) floats
+    for d, C in ((64, 256), (128, 128), (256, 64)):
+        for T in (1, C - 1, C, C + 1, 8192):
+            assert lib.csa_decode_workspace_bytes(3, 5, T, d) == 15 * (T // C + 1) * (d + 2) * 4
+    assert lib.csa_decode_workspace_bytes(0, 5, 10, 64) == 0
+    assert lib.csa_decode_workspace_bytes(1, 1, 10, 96) == -1
+    assert lib.csa_decode_workspace_bytes(1, -1, 10, 64) == -1
+
+
+def test_decode_validation(lib):
+    need = lib.csa_decode_workspace_bytes(2, 2, 300, 128)
+    assert dec(lib, q=NULL) == L.CSA_ERR_INVALID_ARG
+    assert dec(lib, ws=NULL) == L.CSA_ERR_INVALID_ARG
+    assert dec(lib, ws_bytes=need - 1) == L.CSA_ERR_INVALID_ARG
+    assert dec(lib, mode=2) == L.CSA_ERR_INVALID_ARG
+    assert dec(lib, mode=-1) == L.CSA_ERR_INVALID_ARG
+    assert dec(lib, scale=float("nan")) == L.CSA_ERR_INVALID_ARG
+    assert dec(lib, T=0) == L.CSA_ERR_INVALID_ARG  # a query needs its own key
+    assert dec(lib, d=96) == L.CSA_ERR_UNSUPPORTED
+    assert dec(lib, d=0) == L.CSA_ERR_INVALID_ARG
+    assert dec(lib, k=ctypes.c_void_p(4104)) == L.CSA_ERR_ALIGNMENT
+    assert dec(lib, ws=ctypes.c_void_p(4100)) == L.CSA_ERR_ALIGNMENT
+    assert dec(lib, mode=2, k0=ctypes.c_void_p(4098), v0=FAKE) == L.CSA_ERR_ALIGNMENT
+    # empty batch: nothing to do, no pointer needed
+    assert dec(lib, q=NULL, k=NULL, v=NULL, out=NULL, ws=NULL, B=0) == L.CSA_OK
+    import torch
+
+    if not torch.cuda.is_available():
+        assert dec(lib, ws_bytes=need) == L.CSA_ERR_NO_DEVICE
