@@ -187,6 +187,23 @@ int csa_selftest_wait_timeout(unsigned timeout_us, csa_stream_t stream) {
     return from_cuda(csa_tc_selftest_wait_timeout(timeout_us, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int csa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, const void *k0,
+                       const void *v0, const int *seqlens, void *out, float *lse, int B, int H,
+                       int T, int d, float scale, int k0_mode, csa_stream_t stream) {
+    const long long need = csa_decode_scratch_bytes(B, H, T, d);
+    if (need > (long long)CSA_DECODE_NOALLOC_SCRATCH_BYTES) return CSA_ERR_UNSUPPORTED;
+    if (need < 0 || (long long)B * H == 0 || T == 0)  // answered as csa_decode answers them
+        return decode_bf16(q, k_cache, v_cache, k0, v0, seqlens, out, lse, nullptr, 0, B, H, T,
+                           d, scale, k0_mode, stream);
+    int rc = device_ok();
+    if (rc != CSA_OK) return rc;
+    void *scratch = nullptr;
+    if ((rc = csa_decode_noalloc_scratch(&scratch)) != CSA_OK) return rc;
+    return decode_bf16(q, k_cache, v_cache, k0, v0, seqlens, out, lse, scratch,
+                       (long long)CSA_DECODE_NOALLOC_SCRATCH_BYTES, B, H, T, d, scale, k0_mode,
+                       stream);
+}
+
 const char *csa_status_string(int status) {
     switch (status) {
         case CSA_OK: return "ok";

@@ -22,6 +22,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "csa.h"
 #include "csa_device.cuh"
@@ -367,6 +368,31 @@ int csa_decode_run(const void *q, const void *k_cache, const void *v_cache, cons
     if (d == 64) return launch_decode<64>(p, stream);
     if (d == 256) return launch_decode<256>(p, stream);
     return CSA_ERR_UNSUPPORTED;
+}
+
+// Scratch of csa_decode_noalloc: a file-scope device array, so that the
+// entry point allocates nothing.  Its address is looked up once per device.
+static __device__ __align__(256) float g_noalloc_scratch[CSA_DECODE_NOALLOC_SCRATCH_BYTES / 4];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_addr[kMaxDevices];
+}  // namespace
+
+int csa_decode_noalloc_scratch(void **addr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CSA_ERR_NO_DEVICE;
+    if (dev < 0 || dev >= kMaxDevices) return CSA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        // dev is the current device here, so the address is that device's copy.
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return CSA_ERR_CUDA;
+        g_noalloc_addr[dev] = p;
+    }
+    *addr = g_noalloc_addr[dev];
+    return CSA_OK;
 }
 
 int csa_decode_take_status(void) {

@@ -39,3 +39,6 @@ int csa_decode_run(const void *q, const void *k_cache, const void *v_cache, cons
                    const void *v0, const int *seqlens, void *out, float *lse, void *scratch, int B,
                    int H, int T, int d, float scale, int mode, cudaStream_t stream);
 int csa_decode_take_status(void);
+// Address of the file-scope scratch array of csa_decode_noalloc on the
+// current device (looked up once per device).
+int csa_decode_noalloc_scratch(void **addr);

@@ -156,6 +156,29 @@ int csa_decode(const void *q, const void *k_cache, const void *v_cache, const vo
                csa_stream_t stream);
 
 /*
+ * csa_decode_noalloc - csa_decode without a caller workspace.  The method's
+ *   pages have no counterpart to this entry point: it is a convenience of
+ *   this library for callers that cannot hand over scratch memory.
+ *   Same arguments, result, validation and error codes as csa_decode, minus
+ *   workspace and workspace_bytes.  The chunk partials go to a fixed scratch
+ *   array of CSA_DECODE_NOALLOC_SCRATCH_BYTES bytes that lives in the
+ *   library's device image (one per device); the call allocates no memory of
+ *   any kind.  Sizes whose csa_decode_workspace_bytes exceeds that capacity
+ *   are rejected with CSA_ERR_UNSUPPORTED before anything is launched.
+ *   The first call on each device looks the scratch address up with
+ *   cudaGetSymbolAddress (that device must be current): make that first call
+ *   before any stream capture begins.
+ *   Concurrency: every call on a device shares that one scratch array, so
+ *   calls that can overlap on the device (different streams, or several host
+ *   threads) race and corrupt each other's results.  Serialise them, e.g. on
+ *   one stream, or use csa_decode with distinct workspaces.
+ */
+#define CSA_DECODE_NOALLOC_SCRATCH_BYTES (64u << 20)
+int csa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, const void *k0,
+                       const void *v0, const int *seqlens, void *out, float *lse, int B, int H,
+                       int T, int d, float scale, int k0_mode, csa_stream_t stream);
+
+/*
  * csa_decode_workspace_bytes - bytes of workspace csa_decode needs for these
  *   sizes (host only, no device needed), or -1 for a negative size or a d
  *   other than 64, 128, 256.
