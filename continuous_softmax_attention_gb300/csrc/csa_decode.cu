@@ -9,8 +9,9 @@
 // i - 1) are cut into chunks of C positions.  One CTA per (b, h, chunk):
 //   1. stages the chunk's keys plus one halo key on each side (the correction
 //      b of a key needs both neighbours' logits, eq. (10)) and the chunk's
-//      values, with two bulk asynchronous copies;
-//   2. forms the logits, in log2 units, one key per group of d/8 lanes;
+//      values, with two bulk asynchronous copies on separate barriers, so
+//      that the values still load while steps 2 and 3 run;
+//   2. forms the logits, in log2 units, two keys per group of d/8 lanes;
 //   3. forms each key's weight e^{a+b} relative to the chunk's own maximum m:
 //      for a key with logit a and a neighbour at a + x, the neighbour's
 //      interval contributes e^{a-m} phi2(x) (eq. (9));
@@ -34,7 +35,7 @@ using namespace csa_dev;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMergeThreads = 128;
+constexpr int kMergeThreads = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -55,21 +56,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 
 template <int D>
 struct DecCfg {
-    static constexpr int C = 16384 / D;     // positions per chunk: 32 KiB of values
-    static constexpr int KRows = C + 2;      // keys staged: the chunk and a halo key each side
-    static constexpr int LPK = D / 8;        // lanes per key in the logit loop (16 B each)
-    static constexpr int KPW = 32 / LPK;     // keys per warp per step of that loop
-    static constexpr int CP = D / 2;         // column pairs of a value row
-    static constexpr int G = kThreads / CP;  // key groups in the value loop
-    static constexpr int kOffK = 0;
+    static constexpr int KRows = 16384 / D;  // keys staged (32 KiB): the chunk and a halo key each side
+    static constexpr int C = KRows - 2;      // positions per chunk
+    static constexpr int LPK = D / 8;        // lanes per key, 16 bytes (8 columns) each
+    static constexpr int NGrp = kThreads / LPK;  // lane groups in the block
+    static constexpr int kOffK = 0;              // keys; later the value partials [NGrp][D] floats
     static constexpr int kOffV = kOffK + KRows * D * 2;
-    static constexpr int kOffA = kOffV + C * D * 2;       // logits, [KRows] floats
-    static constexpr int kOffW = kOffA + KRows * 4;       // weights, [C] floats
-    static constexpr int kOffRed = kOffW + C * 4;         // value partials, [G][D] floats
-    static constexpr int kOffWarp = kOffRed + G * D * 4;  // block reductions, [2][kWarps]
+    static constexpr int kOffA = kOffV + C * D * 2;   // logits, [KRows] floats
+    static constexpr int kOffW = kOffA + KRows * 4;   // weights, [C] floats
+    static constexpr int kOffWarp = kOffW + C * 4;    // block reductions, [2][kWarps] floats
     static constexpr int kOffBar = (kOffWarp + 2 * kWarps * 4 + 15) / 16 * 16;
-    static constexpr int kSmemBytes = kOffBar + 16;
+    static constexpr int kSmemBytes = kOffBar + 32;  // two mbarriers and the abort flag
     static_assert(kOffV % 16 == 0 && kOffA % 16 == 0, "bulk copy destinations 16-byte aligned");
+    static_assert(NGrp * D * 4 <= KRows * D * 2, "value partials fit in the key buffer");
+    static_assert(KRows % (2 * NGrp) == 0, "the logit loop has no idle lanes");
     static_assert(kSmemBytes <= 75 * 1024, "three CTAs per SM");
 };
 
@@ -94,12 +94,25 @@ __device__ __forceinline__ void unpack8(const uint4 &raw, float (&f)[8]) {
     }
 }
 
-__device__ __forceinline__ float dot8(const float (&q)[8], const uint4 &raw) {
-    float kf[8];
-    unpack8(raw, kf);
+// acc + q.k over the two bf16 pairs of a word each, with the bf16 operands
+// widened exactly inside the fused multiply-add (one rounding per step).
+__device__ __forceinline__ float fma_bf16x2(uint32_t q, uint32_t k, float acc) {
+    asm("{\n\t.reg .b16 ql, qh, kl, kh;\n\t"
+        "mov.b32 {ql, qh}, %1;\n\t"
+        "mov.b32 {kl, kh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, ql, kl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, qh, kh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(q), "r"(k));
+    return acc;
+}
+
+__device__ __forceinline__ float dot8(const uint4 &q, const uint4 &k) {
     float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc = fmaf(q[i], kf[i], acc);
+    acc = fma_bf16x2(q.x, k.x, acc);
+    acc = fma_bf16x2(q.y, k.y, acc);
+    acc = fma_bf16x2(q.z, k.z, acc);
+    acc = fma_bf16x2(q.w, k.w, acc);
     return acc;
 }
 
@@ -110,23 +123,24 @@ __device__ __forceinline__ float dot8(const float (&q)[8], const uint4 &raw) {
 //   x <= 20: pc * (e^x - 1 - x)/x^2, with e^x = 2^{x2};
 //   x > 20:  (2^{un} - pc (1 + x))/x^2, since pc e^x = 2^{un} <= 1 while e^x
 //            alone could overflow.
+// All three are evaluated and one is selected (no divergent branches); the
+// unselected ones may be inf or NaN.
 __device__ __forceinline__ float side_weight(float x2, float un, float pc) {
     const float x = x2 * kLn2;
-    if (fabsf(x) < 1.0f) {
-        float s = 2.505210838544172e-08f;       // 1/11!
-        s = fmaf(s, x, 2.755731922398589e-07f);  // 1/10!
-        s = fmaf(s, x, 2.755731922398589e-06f);  // 1/9!
-        s = fmaf(s, x, 2.48015873015873e-05f);   // 1/8!
-        s = fmaf(s, x, 1.984126984126984e-04f);  // 1/7!
-        s = fmaf(s, x, 1.388888888888889e-03f);  // 1/6!
-        s = fmaf(s, x, 8.333333333333333e-03f);  // 1/5!
-        s = fmaf(s, x, 4.166666666666667e-02f);  // 1/4!
-        s = fmaf(s, x, 1.666666666666667e-01f);  // 1/3!
-        s = fmaf(s, x, 0.5f);                    // 1/2!
-        return pc * s;
-    }
-    if (x <= 20.0f) return pc * ((ex2_approx(x2) - 1.0f - x) / (x * x));
-    return (ex2_approx(un) - pc * (1.0f + x)) / (x * x);
+    float s = 2.505210838544172e-08f;           // 1/11!
+    s = fmaf(s, x, 2.755731922398589e-07f);     // 1/10!
+    s = fmaf(s, x, 2.755731922398589e-06f);     // 1/9!
+    s = fmaf(s, x, 2.48015873015873e-05f);      // 1/8!
+    s = fmaf(s, x, 1.984126984126984e-04f);     // 1/7!
+    s = fmaf(s, x, 1.388888888888889e-03f);     // 1/6!
+    s = fmaf(s, x, 8.333333333333333e-03f);     // 1/5!
+    s = fmaf(s, x, 4.166666666666667e-02f);     // 1/4!
+    s = fmaf(s, x, 1.666666666666667e-01f);     // 1/3!
+    s = fmaf(s, x, 0.5f);                       // 1/2!
+    const float num = x > 20.0f ? ex2_approx(un) - pc * (1.0f + x)
+                                : pc * (ex2_approx(x2) - 1.0f - x);
+    const float direct = num * rcp_approx(x * x);
+    return fabsf(x) < 1.0f ? pc * s : direct;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -140,6 +154,18 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// After an expired wait: keeps the block, and so its shared memory, alive
+// (for at most one more wait limit per barrier) until its copies have landed.
+__device__ __forceinline__ void drain(int tid, uint32_t bar_k, uint32_t bar_v) {
+    if (tid != 0) return;
+    const uint32_t bars[2] = {bar_k, bar_v};
+    for (int i = 0; i < 2; ++i) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bars[i], 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(const DecParams p) {
     using Cf = DecCfg<D>;
@@ -149,10 +175,11 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(const DecParams 
     __nv_bfloat16 *vs = reinterpret_cast<__nv_bfloat16 *>(smem + Cf::kOffV);
     float *as = reinterpret_cast<float *>(smem + Cf::kOffA);
     float *ws = reinterpret_cast<float *>(smem + Cf::kOffW);
-    float *red = reinterpret_cast<float *>(smem + Cf::kOffRed);
+    float *red = reinterpret_cast<float *>(smem + Cf::kOffK);  // after the logits
     float *wred = reinterpret_cast<float *>(smem + Cf::kOffWarp);
-    const uint32_t bar = smem_u32(smem + Cf::kOffBar);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cf::kOffBar + 8);
+    const uint32_t bar_k = smem_u32(smem + Cf::kOffBar);      // keys landed
+    const uint32_t bar_v = smem_u32(smem + Cf::kOffBar + 8);  // values landed
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cf::kOffBar + 16);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int bh = blockIdx.x / p.S, chunk = blockIdx.x - bh * p.S;
@@ -169,63 +196,57 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(const DecParams 
 
     if (tid == 0) {
         *abort_flag = 0;
-        mbar_init(bar, 1);
+        mbar_init(bar_k, 1);
+        mbar_init(bar_v, 1);
         fence_mbar_init();
         const uint32_t kbytes = (uint32_t)(kp_hi - kp_lo + 1) * D * 2;
         const uint32_t vbytes = (uint32_t)(P1 - vp_lo) * D * 2;
-        mbar_arrive_expect_tx(bar, kbytes + vbytes);
-        bulk_load(smem_u32(ks + (kp_lo - P0 + 1) * D), p.k + (head + kp_lo - 1) * D, kbytes, bar);
-        bulk_load(smem_u32(vs + (vp_lo - P0) * D), p.v + (head + vp_lo - 1) * D, vbytes, bar);
+        mbar_arrive_expect_tx(bar_k, kbytes);
+        bulk_load(smem_u32(ks + (kp_lo - P0 + 1) * D), p.k + (head + kp_lo - 1) * D, kbytes, bar_k);
+        mbar_arrive_expect_tx(bar_v, vbytes);
+        bulk_load(smem_u32(vs + (vp_lo - P0) * D), p.v + (head + vp_lo - 1) * D, vbytes, bar_v);
     }
 
-    const int c8 = lane % Cf::LPK;  // this lane's 8 columns of a key
-    float qf[8];
-    unpack8(reinterpret_cast<const uint4 *>(p.q + (size_t)bh * D)[c8], qf);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) qf[i] *= p.qscale;
+    constexpr int LPK = Cf::LPK, NGrp = Cf::NGrp;
+    const int c8 = lane % LPK;  // this lane's 8 columns of a row
+    const int grp = tid / LPK;  // this lane's group
+    const uint4 qraw = reinterpret_cast<const uint4 *>(p.q + (size_t)bh * D)[c8];
 
-    __syncthreads();  // barrier initialised
-    if (!mbar_wait_bounded(bar, 0, abort_flag, &g_dec_status, kWaitLimitNs)) {
-        // Keep the block (and its shared memory) alive until the copies land.
-        if (tid == 0 && !mbar_try_wait(bar, 0)) {
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
-            }
-        }
+    __syncthreads();  // barriers initialised
+    // The values keep loading while the logits and weights are formed.
+    if (!mbar_wait_bounded(bar_k, 0, abort_flag, &g_dec_status, kWaitLimitNs)) {
+        drain(tid, bar_k, bar_v);
         return;
     }
 
-    // The sink's value in slot 0 (chunk 0 only).
-    if (P0 == 0 && tid < D / 8) {
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (p.mode == CSA_K0_GIVEN)
-            val = reinterpret_cast<const uint4 *>(p.v0 + (size_t)h * D)[tid];
-        else if (p.mode == CSA_K0_COPY_FIRST)
-            val = reinterpret_cast<const uint4 *>(vs + D)[tid];
-        reinterpret_cast<uint4 *>(vs)[tid] = val;
-    }
-
-    // Logits of the staged positions [kp_lo - 1 or the sink, kp_hi].
+    // Logits of the staged positions [kp_lo - 1 or the sink, kp_hi]: each
+    // lane group takes two rows per step, ra and rb = ra + NGrp.  Rows
+    // outside that range hold stale data; their logits are never read.
     const int r_lo = (P0 == 0) ? 1 : 0, r_hi = kp_hi - P0 + 1;
-    const int grp = warp * Cf::KPW + lane / Cf::LPK;
-    for (int base = r_lo; base <= r_hi; base += kWarps * Cf::KPW) {
-        const int r = base + grp;
-        float acc = 0.f;
-        if (r <= r_hi) {
-            const int pos = r + P0 - 1;
-            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-            if (pos > 0)
-                raw = reinterpret_cast<const uint4 *>(ks + r * D)[c8];
-            else if (p.mode == CSA_K0_GIVEN)
-                raw = reinterpret_cast<const uint4 *>(p.k0 + (size_t)h * D)[c8];
+#pragma unroll 1
+    for (int base = 0; base < Cf::KRows; base += 2 * NGrp) {
+        if (base > r_hi) break;  // block-uniform
+        const int ra = base + grp, rb = ra + NGrp;
+        uint4 ka = reinterpret_cast<const uint4 *>(ks + ra * D)[c8];
+        const uint4 kb = reinterpret_cast<const uint4 *>(ks + rb * D)[c8];
+        if (P0 == 0 && ra == 1) {  // the sink, position 0
+            if (p.mode == CSA_K0_GIVEN)
+                ka = reinterpret_cast<const uint4 *>(p.k0 + (size_t)h * D)[c8];
             else if (p.mode == CSA_K0_COPY_FIRST)
-                raw = reinterpret_cast<const uint4 *>(ks + 2 * D)[c8];  // position 1
-            acc = dot8(qf, raw);
+                ka = reinterpret_cast<const uint4 *>(ks + 2 * D)[c8];  // position 1
+            else
+                ka = make_uint4(0u, 0u, 0u, 0u);
         }
+        const float pa = dot8(qraw, ka), pb = dot8(qraw, kb);
+        // Reduce-scatter over the group: the lower half ends with row ra's
+        // sum, the upper half with row rb's.
+        const bool upper = (c8 & (LPK / 2)) != 0;
+        float keep = upper ? pb : pa;
+        keep += __shfl_xor_sync(0xffffffffu, upper ? pa : pb, LPK / 2);
 #pragma unroll
-        for (int off = Cf::LPK / 2; off > 0; off >>= 1)
-            acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (r <= r_hi && c8 == 0) as[r] = acc;
+        for (int off = LPK / 4; off > 0; off >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, off);
+        if (c8 == 0) as[ra] = keep * p.qscale;
+        if (c8 == LPK / 2) as[rb] = keep * p.qscale;
     }
     __syncthreads();
 
@@ -256,29 +277,66 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(const DecParams 
     }
     lsum = warp_sum(lsum);
     if (lane == 0) wred[kWarps + warp] = lsum;
+    if (!mbar_wait_bounded(bar_v, 0, abort_flag, &g_dec_status, kWaitLimitNs)) {
+        drain(tid, bar_k, bar_v);
+        return;
+    }
+    // The sink's value in slot 0 (chunk 0 only).
+    if (P0 == 0 && tid < D / 8) {
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (p.mode == CSA_K0_GIVEN)
+            val = reinterpret_cast<const uint4 *>(p.v0 + (size_t)h * D)[tid];
+        else if (p.mode == CSA_K0_COPY_FIRST)
+            val = reinterpret_cast<const uint4 *>(vs + D)[tid];
+        reinterpret_cast<uint4 *>(vs)[tid] = val;
+    }
     __syncthreads();
     lsum = 0.f;
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) lsum += wred[kWarps + i];
 
-    // o = sum_i w_i v_i: G groups of keys, a column pair per thread.
-    const int cp = tid % Cf::CP, g = tid / Cf::CP;
-    float o0 = 0.f, o1 = 0.f;
-    for (int i = g; i < own; i += Cf::G) {
-        const float w = ws[i];
-        const float2 vf =
-            __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(vs + i * D)[cp]);
-        o0 = fmaf(w, vf.x, o0);
-        o1 = fmaf(w, vf.y, o1);
+    // o = sum_i w_i v_i: each lane group takes every NGrp-th key, 8 columns
+    // per lane, two keys per step into two accumulator sets; the groups'
+    // partials meet in the (now unused) key buffer.
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    float acc2[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc2[j] = 0.f;
+    int i = grp;
+    for (; i + NGrp < own; i += 2 * NGrp) {
+        const float w = ws[i], w2 = ws[i + NGrp];
+        const uint4 r1 = reinterpret_cast<const uint4 *>(vs + i * D)[c8];
+        const uint4 r2 = reinterpret_cast<const uint4 *>(vs + (i + NGrp) * D)[c8];
+        float vf[8], vf2[8];
+        unpack8(r1, vf);
+        unpack8(r2, vf2);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            acc[j] = fmaf(w, vf[j], acc[j]);
+            acc2[j] = fmaf(w2, vf2[j], acc2[j]);
+        }
     }
-    reinterpret_cast<float2 *>(red + g * D)[cp] = make_float2(o0, o1);
+    if (i < own) {
+        const float w = ws[i];
+        float vf[8];
+        unpack8(reinterpret_cast<const uint4 *>(vs + i * D)[c8], vf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, vf[j], acc[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] += acc2[j];
+    float4 *dst = reinterpret_cast<float4 *>(red + grp * D + 8 * c8);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     __syncthreads();
     const size_t slot = (size_t)bh * p.S + chunk;
     float *po = p.part_o + slot * D;
     for (int col = tid; col < D; col += kThreads) {
         float s = 0.f;
 #pragma unroll
-        for (int gg = 0; gg < Cf::G; ++gg) s += red[gg * D + col];
+        for (int gg = 0; gg < NGrp; ++gg) s += red[gg * D + col];
         po[col] = s;
     }
     if (tid == 0) {
@@ -287,10 +345,18 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(const DecParams 
     }
 }
 
+// One block per (b, h).  The chunk maxima reduce to M across the block; the
+// chunk factors 2^{m_c - M} go to shared memory a tile at a time, and each
+// output column sums its chunks' partials (kParts threads per column, loads
+// coalesced across columns).
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecParams p) {
     constexpr int C = DecCfg<D>::C;
-    const int bh = blockIdx.x, b = bh / p.H, tid = threadIdx.x;
+    constexpr int kParts = kMergeThreads / D, kTile = 1024, kMW = kMergeThreads / 32;
+    __shared__ float fac[kTile];
+    __shared__ float red[2][kMW];
+    __shared__ float part[kParts][D];
+    const int bh = blockIdx.x, b = bh / p.H, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = p.seqlens ? p.seqlens[b] : p.T;
     __nv_bfloat16 *out = p.out + (size_t)bh * D;
     if (n < 1 || n > p.T) {  // a length outside [1, T]: NaN result, status word set
@@ -305,14 +371,40 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecPa
     const float *ml = p.part_ml + (size_t)bh * p.S * 2;
     const float *po = p.part_o + (size_t)bh * p.S * D;
     float M = -INFINITY;
-    for (int c = 0; c < nch; ++c) M = fmaxf(M, ml[2 * c]);
-    float L = 0.f;
-    for (int c = 0; c < nch; ++c) L = fmaf(ml[2 * c + 1], ex2_approx(ml[2 * c] - M), L);
-    const float inv = 1.0f / L;
-    for (int col = tid; col < D; col += kMergeThreads) {
-        float acc = 0.f;
-        for (int c = 0; c < nch; ++c) acc = fmaf(po[(size_t)c * D + col], ex2_approx(ml[2 * c] - M), acc);
-        out[col] = __float2bfloat16_rn(acc * inv);
+    for (int c = tid; c < nch; c += kMergeThreads) M = fmaxf(M, ml[2 * c]);
+    M = warp_max(M);
+    if (lane == 0) red[0][warp] = M;
+    __syncthreads();
+    M = red[0][0];
+#pragma unroll
+    for (int i = 1; i < kMW; ++i) M = fmaxf(M, red[0][i]);
+    const int col = tid % D, prt = tid / D;
+    float acc = 0.f, L = 0.f;
+    for (int t0 = 0; t0 < nch; t0 += kTile) {
+        const int tn = min(kTile, nch - t0);
+        for (int c = tid; c < tn; c += kMergeThreads) {
+            const float f = ex2_approx(ml[2 * (t0 + c)] - M);
+            fac[c] = f;
+            L = fmaf(ml[2 * (t0 + c) + 1], f, L);
+        }
+        __syncthreads();
+        const float *pt = po + (size_t)t0 * D + col;
+#pragma unroll 4
+        for (int c = prt; c < tn; c += kParts) acc = fmaf(pt[(size_t)c * D], fac[c], acc);
+        __syncthreads();
+    }
+    L = warp_sum(L);
+    if (lane == 0) red[1][warp] = L;
+    part[prt][col] = acc;
+    __syncthreads();
+    L = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMW; ++i) L += red[1][i];
+    if (prt == 0) {
+        float s = acc;
+#pragma unroll
+        for (int i = 1; i < kParts; ++i) s += part[i][col];
+        out[col] = __float2bfloat16_rn(s * (1.0f / L));
     }
     if (tid == 0 && p.lse) p.lse[bh] = (M + log2f(L)) * kLn2;
 }

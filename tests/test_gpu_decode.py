@@ -3,7 +3,7 @@
 The decode output of sequence b is row n_b - 1 of eq. (8) over the first n_b
 tokens; the oracle computes exactly that row, from the same bf16 values, on
 a [1, 1, n_b, d] slice whose last query row is the decode query.  Lengths are
-picked around the kernel's chunk edges (C = 16384 / d positions, position 0
+picked around the kernel's chunk edges (C = 16384 / d - 2 positions, position 0
 being the sink), so that the halo keys across chunks and the one-sided end
 terms of eq. (10) are all exercised."""
 import numpy as np
@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 
 def chunk(d):
-    return 16384 // d
+    return 16384 // d - 2
 
 
 def oracle_decode(x, seqlens, scale, mode, pairs):
@@ -80,7 +80,8 @@ def test_decode_chunk_edges(d, mode):
 def test_decode_logit_ranges(scale):
     # scale 4 at d = 64 gives logit gaps of order +-100 between neighbours
     d, T = 64, 700
-    lens = [1, 255, 256, 257, 513, 700]
+    C = chunk(d)
+    lens = [1, C - 1, C, C + 1, 2 * C + 1, T]
     x = make_decode_inputs(len(lens), 3, T, d, seed=31)
     pairs = [(b, h) for b in range(len(lens)) for h in range(3)]
     o, lse = run_decode(x, lens, scale, 0)
