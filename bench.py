@@ -62,35 +62,44 @@ def _dist_env():
 
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "csa_forward_headline.md")
 KERNEL_SOURCES = ["csa_tc.cu", "csa_tc_common.cuh", "csa_device.cuh"]
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_chunk_bench.md")
+DECODE_SOURCES = ["csa_decode.cu", "csa_device.cuh"]
 
 
-def kernel_source_hash():
-    """sha256 over the sources of the continuous tensor-core kernel."""
+def kernel_source_hash(names=KERNEL_SOURCES):
+    """sha256 over the sources of one kernel."""
     import hashlib
 
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in names:
         with open(os.path.join(ROOT, "continuous_softmax_attention_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def recorded_traffic():
-    """DRAM bytes per launch of the headline kernel from the committed ncu
-    summary, or None when the kernel sources changed since it was taken."""
+def recorded_figure(path, key, sources):
+    """A figure recorded in a committed ncu summary (lines `key: value` and
+    `source_sha256: ...`), or None when the kernel's sources changed since
+    the counters were taken."""
     try:
         fields = {}
-        with open(PROFILE_SUMMARY) as f:
+        with open(path) as f:
             for line in f:
                 line = line.strip().strip("`")
-                for key in ("traffic_bytes_per_launch:", "source_sha256:"):
-                    if line.startswith(key):
-                        fields[key] = line[len(key):].strip()
-        if fields.get("source_sha256:") != kernel_source_hash():
+                for k in (key + ":", "source_sha256:"):
+                    if line.startswith(k):
+                        fields[k] = line[len(k):].strip()
+        if fields.get("source_sha256:") != kernel_source_hash(sources):
             return None
-        return int(fields["traffic_bytes_per_launch:"])
+        return float(fields[key + ":"])
     except Exception:
         return None
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the headline kernel, or None."""
+    v = recorded_figure(PROFILE_SUMMARY, "traffic_bytes_per_launch", KERNEL_SOURCES)
+    return None if v is None else int(v)
 
 
 def _peaks():
@@ -354,6 +363,8 @@ class DecodeBench:
         except Exception:
             peak, src = 6800.0, "fallback"
         achieved = self.bytes / (ms * 1e-3) / 1e9
+        per_pos = recorded_figure(DECODE_PROFILE, "traffic_bytes_per_position", DECODE_SOURCES)
+        traffic = None if per_pos is None else int(per_pos * sum(self.lens) * w.H)
         h2d = self.pin_q.numel() * self.pin_q.element_size()
         d2h = (self.host_out.numel() * self.host_out.element_size() +
                self.host_lse.numel() * self.host_lse.element_size())
@@ -367,7 +378,9 @@ class DecodeBench:
                        f"{2 * sum(self.lens) * w.H * w.d * 2 / 2**30:.2f} GiB > L2"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "peak_source": f"{src} copy bandwidth", "traffic": None,
+                         "peak_source": f"{src} copy bandwidth", "traffic": traffic,
+                         "traffic_unit": "bytes per call (ncu dram read+write of the chunk "
+                                         "kernel per (b, h, position), times this workload's)",
                          "algorithmic_bytes": self.bytes,
                          "timed": "whole csa_decode call (chunk kernel + merge kernel)"},
             "e2e": {"value": round(gbs_e2e, 2), "unit": "GB/s", "ms_per_step": round(tot_e2e / steps, 5),
