@@ -16,6 +16,10 @@ What it computes follows Jianlin Su, "Continuous Softmax Attention"
 * ``row_bias``       - the logits ``a`` and corrections ``b`` of eq. (10)
                        for one row.
 * ``phi1``/``phi2``/``log_phi1``/``log_phi2`` - eq. (6) and its limits.
+* ``backward``       - gradients of eq. (10)/(11) with respect to q, k, v
+                       and the trainable sink pair, by the plain chain rule
+                       (``csa_oracle_backward.c``); ``log_dphi2`` is
+                       log phi2'(x), the derivative it needs.
 * ``oracle.quadrature.forward`` - eq. (2) itself by composite Gauss-Legendre
                        quadrature over the linearly interpolated keys and
                        values of eq. (3); it uses no phi function.
@@ -30,7 +34,7 @@ import os
 
 import numpy as np
 
-from .build import LIB_PATH, build_oracle
+from .build import LIB_PATH, SOURCES, build_oracle
 
 ZERO, COPY_FIRST, GIVEN = 0, 1, 2
 
@@ -41,9 +45,8 @@ def _load():
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < os.path.getmtime(
-        os.path.join(os.path.dirname(__file__), "csa_oracle.c")
-    ):
+    if not os.path.exists(LIB_PATH) or any(
+            os.path.getmtime(LIB_PATH) < os.path.getmtime(src) for src in SOURCES):
         build_oracle()
     lib = ctypes.CDLL(LIB_PATH)
     d = ctypes.c_double
@@ -67,6 +70,10 @@ def _load():
     lib.csa_oracle_std_forward_rows.restype = i
     lib.csa_oracle_row_bias.argtypes = [p, p, p, i, i, i, i, d, i, i, i, i, p, p]
     lib.csa_oracle_row_bias.restype = i
+    lib.csa_oracle_log_dphi2.restype = d
+    lib.csa_oracle_log_dphi2.argtypes = [d]
+    lib.csa_oracle_backward.argtypes = [p, p, p, p, p, p, p, p, p, p, p, i, i, i, i, d, i, i]
+    lib.csa_oracle_backward.restype = i
     _lib = lib
     return lib
 
@@ -210,3 +217,33 @@ def row_bias(q, k, b, h, r, k0=None, scale=None, mode=ZERO):
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
     return a, bb
+
+
+def log_dphi2(x: float) -> float:
+    """log phi2'(x), phi2'(x) = int_0^1 s (1 - s) e^{sx} ds."""
+    return _load().csa_oracle_log_dphi2(float(x))
+
+
+def backward(q, k, v, dout, k0=None, v0=None, scale=None, mode=ZERO, nthreads=None):
+    """Gradients of L = sum(dout * o) for the continuous forward pass.
+
+    Returns dict(dq, dk, dv, dk0, dv0) of float64 arrays ([B, H, T, d], and
+    [H, d] for the sink pair in mode GIVEN, else None)."""
+    q, k, v, k0, v0, (B, H, T, d) = _prep(q, k, v, k0, v0, mode)
+    g = _f32(dout)
+    if g.shape != q.shape:
+        raise ValueError("dout must be [B, H, T, d]")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dq = np.zeros((B, H, T, d), dtype=np.float64)
+    dk = np.zeros_like(dq)
+    dv = np.zeros_like(dq)
+    dk0 = np.zeros((H, d), dtype=np.float64) if mode == GIVEN else None
+    dv0 = np.zeros((H, d), dtype=np.float64) if mode == GIVEN else None
+    rc = _load().csa_oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(k0), _ptr(v0), _ptr(g),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dk0), _ptr(dv0),
+                                     B, H, T, d, float(scale), int(mode),
+                                     int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return {"dq": dq, "dk": dk, "dv": dv, "dk0": dk0, "dv0": dv0}

@@ -9,14 +9,14 @@ import os
 import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-SRC = os.path.join(HERE, "csa_oracle.c")
+SOURCES = [os.path.join(HERE, "csa_oracle.c"), os.path.join(HERE, "csa_oracle_backward.c")]
 LIB_PATH = os.path.join(HERE, "libcsa_oracle.so")
 
 
 def build_oracle(verbose: bool = False) -> str:
     cc = os.environ.get("CC", "gcc")
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [cc, "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-Wall", "-o", tmp, SRC, "-lm"]
+    cmd = [cc, "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-Wall", "-o", tmp] + SOURCES + ["-lm"]
     if verbose:
         print(" ".join(cmd))
     subprocess.run(cmd, check=True)
