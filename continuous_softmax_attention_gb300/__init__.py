@@ -8,7 +8,10 @@ loudly when the library has not been built.
 from .inputs import ZERO, COPY_FIRST, GIVEN  # noqa: F401
 from ._lib import (  # noqa: F401
     CsaError,
+    backward,
+    backward_workspace_bytes,
     decode,
+    decode_noalloc,
     decode_workspace_bytes,
     device_status,
     forward,
@@ -20,7 +23,7 @@ from ._lib import (  # noqa: F401
 )
 
 __all__ = [
-    "ZERO", "COPY_FIRST", "GIVEN", "CsaError", "forward", "std_forward", "decode",
-    "decode_workspace_bytes", "logphi2_eval",
+    "ZERO", "COPY_FIRST", "GIVEN", "CsaError", "forward", "std_forward", "backward",
+    "backward_workspace_bytes", "decode", "decode_noalloc", "decode_workspace_bytes", "logphi2_eval",
     "segment_weights_eval", "device_status", "selftest_wait_timeout", "status_string",
 ]

@@ -47,6 +47,7 @@ def load():
     p, i, f, u = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint
     fwd = [p, p, p, p, p, p, p, i, i, i, i, f, i, p]
     std = [p, p, p, p, p, i, i, i, i, f, p]
+    bwd = [p, p, p, p, p, p, p, p, p, p, p, p, p, p, ctypes.c_longlong, i, i, i, i, f, i, p]
     for name, args in (("csa_forward", fwd), ("csa_forward_f32", fwd),
                        ("csa_std_forward", std), ("csa_std_forward_f32", std),
                        ("csa_logphi2_eval", [p, p, i, p]),
@@ -55,12 +56,15 @@ def load():
                        ("csa_selftest_wait_timeout", [u, p]),
                        ("csa_abi_version", []),
                        ("csa_decode", [p, p, p, p, p, p, p, p, p, ctypes.c_longlong, i, i, i, i,
-                                       f, i, p])):
+                                       f, i, p]),
+                       ("csa_decode_noalloc", [p, p, p, p, p, p, p, p, i, i, i, i, f, i, p]),
+                       ("csa_backward", bwd), ("csa_backward_f32", bwd)):
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = i
-    lib.csa_decode_workspace_bytes.argtypes = [i, i, i, i]
-    lib.csa_decode_workspace_bytes.restype = ctypes.c_longlong
+    for name in ("csa_decode_workspace_bytes", "csa_backward_workspace_bytes"):
+        getattr(lib, name).argtypes = [i, i, i, i]
+        getattr(lib, name).restype = ctypes.c_longlong
     lib.csa_status_string.argtypes = [i]
     lib.csa_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -234,6 +238,103 @@ def decode(q, k_cache, v_cache, k0=None, v0=None, *, seqlens=None, mode: int = 0
                              _ptr(seqlens), _ptr(out), _ptr(lse), _ptr(workspace), nbytes, B, H,
                              T, d, float(scale), int(mode), _stream_handle(stream)), "csa_decode")
     return out, lse
+
+
+def decode_noalloc(q, k_cache, v_cache, k0=None, v0=None, *, seqlens=None, mode: int = 0,
+                   scale=None, out=None, lse=None, stream=None, want_lse: bool = True):
+    """decode() through csa_decode_noalloc: no workspace, the library's fixed
+    device scratch array instead (calls on one device must not overlap)."""
+    import torch
+
+    B, H, T, d = k_cache.shape
+    dev = k_cache.device
+    bf = torch.bfloat16
+    _check_tensor(k_cache, "k_cache", bf, (B, H, T, d), dev)
+    _check_tensor(v_cache, "v_cache", bf, (B, H, T, d), dev)
+    _check_tensor(q, "q", bf, (B, H, d), dev)
+    if mode == 2:
+        if k0 is None or v0 is None:
+            raise ValueError("mode 2 (given sink) needs k0 and v0")
+        _check_tensor(k0, "k0", bf, (H, d), dev)
+        _check_tensor(v0, "v0", bf, (H, d), dev)
+    else:
+        k0 = v0 = None
+    if seqlens is not None:
+        _check_tensor(seqlens, "seqlens", torch.int32, (B,), dev)
+    if scale is None:
+        scale = 1.0 / d ** 0.5
+    if out is None:
+        out = torch.empty((B, H, d), dtype=bf, device=dev)
+    _check_tensor(out, "out", bf, (B, H, d), dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _check_tensor(lse, "lse", torch.float32, (B, H), dev)
+    _check(load().csa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k0), _ptr(v0),
+                                     _ptr(seqlens), _ptr(out), _ptr(lse), B, H, T, d,
+                                     float(scale), int(mode), _stream_handle(stream)),
+           "csa_decode_noalloc")
+    return out, lse
+
+
+def backward_workspace_bytes(B: int, H: int, T: int, d: int) -> int:
+    """Bytes of workspace csa_backward needs (host-side, no device needed)."""
+    n = int(load().csa_backward_workspace_bytes(int(B), int(H), int(T), int(d)))
+    if n < 0:
+        raise CsaError(CSA_ERR_UNSUPPORTED, "csa_backward_workspace_bytes")
+    return n
+
+
+def backward(q, k, v, out, lse, dout, k0=None, v0=None, *, mode: int = 0, scale=None,
+             dq=None, dk=None, dv=None, dk0=None, dv0=None, workspace=None, stream=None):
+    """Gradients of the continuous forward pass for the upstream gradient
+    dout.  q, k, v, out, dout: CUDA [B, H, T, d], all bf16 or all fp32; lse:
+    float32 [B, H, T] from forward().  Returns (dq, dk, dv, dk0, dv0); dk0 and
+    dv0 (float32 [H, d]) are None unless mode is GIVEN (2)."""
+    import torch
+
+    B, H, T, d = q.shape
+    dtype, dev = q.dtype, q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _check_tensor(t, name, dtype, (B, H, T, d), dev)
+    _check_tensor(lse, "lse", torch.float32, (B, H, T), dev)
+    if mode == 2:
+        if k0 is None or v0 is None:
+            raise ValueError("mode 2 (given sink) needs k0 and v0")
+        _check_tensor(k0, "k0", dtype, (H, d), dev)
+        _check_tensor(v0, "v0", dtype, (H, d), dev)
+        if dk0 is None:
+            dk0 = torch.empty((H, d), dtype=torch.float32, device=dev)
+        if dv0 is None:
+            dv0 = torch.empty((H, d), dtype=torch.float32, device=dev)
+        _check_tensor(dk0, "dk0", torch.float32, (H, d), dev)
+        _check_tensor(dv0, "dv0", torch.float32, (H, d), dev)
+    else:
+        k0 = v0 = dk0 = dv0 = None
+    if scale is None:
+        scale = 1.0 / d ** 0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_tensor(t, name, dtype, (B, H, T, d), dev)
+    if workspace is None:
+        workspace = torch.empty(max(backward_workspace_bytes(B, H, T, d), 16), dtype=torch.uint8,
+                                device=dev)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on q's device")
+    nbytes = workspace.numel() * workspace.element_size()
+    lib = load()
+    if dtype == torch.bfloat16:
+        fn, where = lib.csa_backward, "csa_backward"
+    elif dtype == torch.float32:
+        fn, where = lib.csa_backward_f32, "csa_backward_f32"
+    else:
+        raise ValueError(f"unsupported dtype {dtype}")
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(k0), _ptr(v0), _ptr(out), _ptr(lse), _ptr(dout),
+              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dk0), _ptr(dv0), _ptr(workspace), nbytes, B, H,
+              T, d, float(scale), int(mode), _stream_handle(stream)), where)
+    return dq, dk, dv, dk0, dv0
 
 
 def logphi2_eval(x, stream=None):

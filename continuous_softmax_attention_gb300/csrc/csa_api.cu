@@ -111,9 +111,81 @@ int decode_bf16(const void *q, const void *k_cache, const void *v_cache, const v
                           scale, mode, reinterpret_cast<cudaStream_t>(stream));
 }
 
+long long backward_scratch_bytes(int B, int H, int T, int d) {
+    if (B < 0 || H < 0 || T < 0 || d < 1 || d > 256) return -1;
+    return csa_simt_backward_scratch_bytes(B, H, T, d);
+}
+
+int backward_any(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+                 const void *out, const float *lse, const void *dout, void *dq, void *dk,
+                 void *dv, float *dk0, float *dv0, void *workspace, long long workspace_bytes,
+                 int B, int H, int T, int d, float scale, int mode, bool bf16,
+                 csa_stream_t stream) {
+    bool empty;
+    int rc = check_common(q, k, v, k0, v0, out, B, H, T, d, scale, mode, true, &empty);
+    if (rc != CSA_OK) return rc;
+    if (empty) {
+        // nothing to differentiate; the sink gradients are zero
+        if (mode == CSA_K0_GIVEN && (long long)H * d > 0) {
+            if (!dk0 || !dv0) return CSA_ERR_INVALID_ARG;
+            if ((rc = device_ok()) != CSA_OK) return rc;
+            cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+            if (cudaMemsetAsync(dk0, 0, sizeof(float) * (size_t)H * d, s) != cudaSuccess ||
+                cudaMemsetAsync(dv0, 0, sizeof(float) * (size_t)H * d, s) != cudaSuccess)
+                return CSA_ERR_CUDA;
+        }
+        return CSA_OK;
+    }
+    if (!lse || !dout || !dq || !dk || !dv || !workspace) return CSA_ERR_INVALID_ARG;
+    if (mode == CSA_K0_GIVEN && (!dk0 || !dv0)) return CSA_ERR_INVALID_ARG;
+    if (d > 256) return CSA_ERR_UNSUPPORTED;
+    const long long need = backward_scratch_bytes(B, H, T, d);
+    if (need < 0) return CSA_ERR_UNSUPPORTED;
+    if (workspace_bytes < need) return CSA_ERR_INVALID_ARG;
+    const uintptr_t al = bf16 ? 2 : 4;
+    if (!aligned(q, al) || !aligned(k, al) || !aligned(v, al) || !aligned(out, al) ||
+        !aligned(dout, al) || !aligned(dq, al) || !aligned(dk, al) || !aligned(dv, al) ||
+        !aligned(lse, 4) || !aligned(workspace, 16) ||
+        (mode == CSA_K0_GIVEN && (!aligned(k0, al) || !aligned(v0, al) || !aligned(dk0, 4) ||
+                                  !aligned(dv0, 4))))
+        return CSA_ERR_ALIGNMENT;
+    if ((rc = device_ok()) != CSA_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (bf16)
+        return from_cuda(csa_simt_backward_bf16(q, k, v, k0, v0, out, lse, dout, dq, dk, dv, dk0,
+                                                dv0, workspace, B, H, T, d, scale, mode, s));
+    return from_cuda(csa_simt_backward_f32(
+        static_cast<const float *>(q), static_cast<const float *>(k),
+        static_cast<const float *>(v), static_cast<const float *>(k0),
+        static_cast<const float *>(v0), static_cast<const float *>(out), lse,
+        static_cast<const float *>(dout), static_cast<float *>(dq), static_cast<float *>(dk),
+        static_cast<float *>(dv), dk0, dv0, workspace, B, H, T, d, scale, mode, s));
+}
+
 }  // namespace
 
 extern "C" {
+
+long long csa_backward_workspace_bytes(int B, int H, int T, int d) {
+    return backward_scratch_bytes(B, H, T, d);
+}
+
+int csa_backward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+                 const void *out, const float *lse, const void *dout, void *dq, void *dk,
+                 void *dv, float *dk0, float *dv0, void *workspace, long long workspace_bytes,
+                 int B, int H, int T, int d, float scale, int k0_mode, csa_stream_t stream) {
+    return backward_any(q, k, v, k0, v0, out, lse, dout, dq, dk, dv, dk0, dv0, workspace,
+                        workspace_bytes, B, H, T, d, scale, k0_mode, true, stream);
+}
+
+int csa_backward_f32(const float *q, const float *k, const float *v, const float *k0,
+                     const float *v0, const float *out, const float *lse, const float *dout,
+                     float *dq, float *dk, float *dv, float *dk0, float *dv0, void *workspace,
+                     long long workspace_bytes, int B, int H, int T, int d, float scale,
+                     int k0_mode, csa_stream_t stream) {
+    return backward_any(q, k, v, k0, v0, out, lse, dout, dq, dk, dv, dk0, dv0, workspace,
+                        workspace_bytes, B, H, T, d, scale, k0_mode, false, stream);
+}
 
 long long csa_decode_workspace_bytes(int B, int H, int T, int d) {
     return csa_decode_scratch_bytes(B, H, T, d);

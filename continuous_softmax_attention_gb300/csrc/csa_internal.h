@@ -42,3 +42,17 @@ int csa_decode_take_status(void);
 // Address of the file-scope scratch array of csa_decode_noalloc on the
 // current device (looked up once per device).
 int csa_decode_noalloc_scratch(void **addr);
+
+// Backward pass on CUDA cores (csa_bwd_simt.cu), any d <= 256.  scratch
+// holds csa_simt_backward_scratch_bytes bytes (fp32 dk, dv accumulators).
+long long csa_simt_backward_scratch_bytes(int B, int H, int T, int d);
+cudaError_t csa_simt_backward_f32(const float *q, const float *k, const float *v, const float *k0,
+                                  const float *v0, const float *o, const float *lse,
+                                  const float *dout, float *dq, float *dk, float *dv, float *dk0,
+                                  float *dv0, void *scratch, int B, int H, int T, int d,
+                                  float scale, int mode, cudaStream_t stream);
+cudaError_t csa_simt_backward_bf16(const void *q, const void *k, const void *v, const void *k0,
+                                   const void *v0, const void *o, const float *lse,
+                                   const void *dout, void *dq, void *dk, void *dv, float *dk0,
+                                   float *dv0, void *scratch, int B, int H, int T, int d,
+                                   float scale, int mode, cudaStream_t stream);

@@ -119,6 +119,55 @@ int csa_std_forward_f32(const float *q, const float *k, const float *v, float *o
                         int B, int H, int T, int d, float scale, csa_stream_t stream);
 
 /*
+ * csa_backward - gradients of the continuous forward pass (csa_forward) for
+ *   an upstream gradient dout = dL/d(out): dq, dk, dv and, in CSA_K0_GIVEN
+ *   mode, the gradients of the trainable sink pair.
+ *   Defines: the derivative of eq. (10)/(11) of "Continuous Softmax
+ *   Attention" ("Assembly and Simplification"); the pages train models with
+ *   the method ("Simple Experiments") but do not write this step out.  With
+ *   p_i = e^{a_i - lse}, P_i the attention weight e^{a_i + b_i - lse},
+ *   dP_i = dout . v_i and D = dout . out, for every row
+ *       dL/da_i = P_i (dP_i - D) + F_i - F_{i+1},
+ *       F_i = c_i (dP_{i-1} - dP_i),  c_i = p_{i-1} phi2'(a_i - a_{i-1}),
+ *   (F = 0 past both ends of the row; phi2' is the derivative of eq. (6)'s
+ *   phi2), and dq = scale sum_i dL/da_i k_i, dk_i += scale dL/da_i q,
+ *   dv_i += P_i dout.
+ *   q, k, v, out, dout: bf16 [B, H, T, d] (out from csa_forward);
+ *   lse: float [B, H, T] from csa_forward (required);
+ *   dq, dk, dv: bf16 [B, H, T, d], overwritten;
+ *   k0, v0: bf16 [H, d] (CSA_K0_GIVEN only); dk0, dv0: float [H, d], the
+ *   gradients of the sink pair summed over the batch and the rows
+ *   (CSA_K0_GIVEN only; may be NULL otherwise).  In CSA_K0_COPY_FIRST the
+ *   sink's gradient is added to key 0's; in CSA_K0_ZERO the sink is a
+ *   constant.
+ *   workspace: DEVICE scratch of at least csa_backward_workspace_bytes(B, H,
+ *   T, d) bytes, 16-byte aligned, contents on entry irrelevant.  Concurrent
+ *   calls need distinct workspaces.
+ *   1 <= d <= 256 (CSA_ERR_UNSUPPORTED otherwise).  Tensors 2-byte aligned,
+ *   lse, dk0, dv0 4-byte aligned.  Empty problems (B, H or T = 0) are
+ *   CSA_OK; in CSA_K0_GIVEN mode dk0 and dv0 are then zeroed.  Atomic
+ *   accumulation makes the low bits of dk, dv, dk0, dv0 depend on the order
+ *   in which the hardware completes them.
+ */
+int csa_backward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+                 const void *out, const float *lse, const void *dout, void *dq, void *dk,
+                 void *dv, float *dk0, float *dv0, void *workspace, long long workspace_bytes,
+                 int B, int H, int T, int d, float scale, int k0_mode, csa_stream_t stream);
+
+/* csa_backward_f32 - the same in fp32 throughout (CUDA cores, no TF32); all
+ * tensors 4-byte aligned. */
+int csa_backward_f32(const float *q, const float *k, const float *v, const float *k0,
+                     const float *v0, const float *out, const float *lse, const float *dout,
+                     float *dq, float *dk, float *dv, float *dk0, float *dv0, void *workspace,
+                     long long workspace_bytes, int B, int H, int T, int d, float scale,
+                     int k0_mode, csa_stream_t stream);
+
+/* csa_backward_workspace_bytes - workspace bytes csa_backward and
+ * csa_backward_f32 need (host only), or -1 for a negative size or d outside
+ * 1..256. */
+long long csa_backward_workspace_bytes(int B, int H, int T, int d);
+
+/*
  * csa_decode - one decode step: for every sequence b and head h, the output
  *   of the newest token, position t = n_b, against the sink and the n_b
  *   cached keys and values.

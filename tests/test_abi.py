@@ -131,3 +131,29 @@ def test_decode_validation(lib):
 
     if not torch.cuda.is_available():
         assert dec(lib, ws_bytes=need) == L.CSA_ERR_NO_DEVICE
+
+
+def bwd(lib, *, q=FAKE, k=FAKE, v=FAKE, k0=NULL, v0=NULL, out=FAKE, lse=FAKE, dout=FAKE,
+        dq=FAKE, dk=FAKE, dv=FAKE, dk0=NULL, dv0=NULL, ws=FAKE, ws_bytes=1 << 30, B=1, H=2, T=8,
+        d=64, scale=0.1, mode=0):
+    return lib.csa_backward(q, k, v, k0, v0, out, lse, dout, dq, dk, dv, dk0, dv0, ws, ws_bytes,
+                            B, H, T, d, scale, mode, None)
+
+
+def test_backward_validation(lib):
+    need = lib.csa_backward_workspace_bytes(1, 2, 8, 64)
+    assert need == 2 * 1 * 2 * 8 * 64 * 4  # fp32 dk, dv accumulators
+    assert lib.csa_backward_workspace_bytes(1, 1, 1, 257) == -1
+    assert bwd(lib, lse=NULL) == L.CSA_ERR_INVALID_ARG
+    assert bwd(lib, dout=NULL) == L.CSA_ERR_INVALID_ARG
+    assert bwd(lib, ws=NULL) == L.CSA_ERR_INVALID_ARG
+    assert bwd(lib, ws_bytes=need - 1) == L.CSA_ERR_INVALID_ARG
+    assert bwd(lib, mode=2, k0=FAKE, v0=FAKE) == L.CSA_ERR_INVALID_ARG  # no dk0/dv0
+    assert bwd(lib, d=300) == L.CSA_ERR_UNSUPPORTED
+    assert bwd(lib, dq=ctypes.c_void_p(4097)) == L.CSA_ERR_ALIGNMENT
+    assert bwd(lib, q=NULL, k=NULL, v=NULL, out=NULL, lse=NULL, dout=NULL, dq=NULL, dk=NULL,
+               dv=NULL, ws=NULL, T=0) == L.CSA_OK
+    import torch
+
+    if not torch.cuda.is_available():
+        assert bwd(lib, ws_bytes=need) == L.CSA_ERR_NO_DEVICE
