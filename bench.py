@@ -217,6 +217,7 @@ def run_gpu(args):
     std_call = lambda: csa.std_forward(g["q"], g["k"], g["v"], scale=scale, out=out, lse=lse)
 
     dec = None if args.no_decode else DecodeBench(csa, dev, stream, flush)
+    bwd = None if args.no_backward else BackwardBench(csa, g, out, lse, scale, w.modes[0], dev)
 
     # end to end through the C ABI with host buffers
     pin = {k: x[k].pin_memory() for k in ("q", "k", "v")}
@@ -242,6 +243,8 @@ def run_gpu(args):
         if dec is not None:
             dec.call()
             dec.e2e_call()
+        if bwd is not None:
+            bwd.call()
     torch.cuda.synchronize()
     assert csa.device_status() == 0
 
@@ -254,6 +257,8 @@ def run_gpu(args):
         if dec is not None:
             dec.ms = timed(dec.call, args.decode_steps)
             dec.ms_e2e = timed(dec.e2e_call, args.decode_steps)
+        if bwd is not None:
+            bwd.ms = timed(bwd.call, args.backward_steps)
     barrier()
     t_wall = time.perf_counter() - t_wall
     status = csa.device_status()
@@ -296,7 +301,8 @@ def run_gpu(args):
                 "ratio_continuous_over_std": round(value / std_value, 4)},
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "ms_per_step": round(tot_e2e / K, 5),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 3 * K + (0 if dec is None else 2 * 2 * args.decode_steps),
+        "gpu_launches": 3 * K + (0 if dec is None else 2 * 2 * args.decode_steps) +
+                        (0 if bwd is None else bwd.launches * args.backward_steps),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": burst,
                      "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
                      "peak_source": f"{src} bf16 dense (burst)", "traffic": recorded_traffic(),
@@ -308,9 +314,60 @@ def run_gpu(args):
     }
     if dec is not None:
         line["decode"] = dec.summary(ws, args.decode_steps, max_over_ranks, dev)
+    if bwd is not None:
+        line["backward"] = bwd.summary(ws, args.backward_steps, max_over_ranks, dev, burst, src)
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = cpu_baseline(x, scale, budget_s=args.cpu_seconds)
     return line
+
+
+class BackwardBench:
+    """The backward pass at the headline shape: dq, dk, dv from q, k, v, the
+    forward's out and lse, and a seeded upstream gradient (inputs resident)."""
+
+    launches = 3  # D row dot, the tensor-core kernel, the dq conversion
+
+    def __init__(self, csa, g, out, lse, scale, mode, dev):
+        import torch
+
+        self.csa, self.g, self.scale, self.mode = csa, g, scale, mode
+        B, H, T, d = g["q"].shape
+        gen = torch.Generator().manual_seed(7)
+        self.dout = torch.randn(B, H, T, d, generator=gen).to(torch.bfloat16).to(dev)
+        self.out = torch.empty_like(out)
+        self.lse = torch.empty_like(lse)
+        csa.forward(g["q"], g["k"], g["v"], mode=mode, scale=scale, out=self.out, lse=self.lse)
+        self.grads = [torch.empty_like(g["q"]) for _ in range(3)]
+        self.ws = torch.empty(csa.backward_workspace_bytes(B, H, T, d), dtype=torch.uint8,
+                              device=dev)
+        self.shape = (B, H, T, d)
+        self.ms = None
+
+    def call(self):
+        g = self.g
+        self.csa.backward(g["q"], g["k"], g["v"], self.out, self.lse, self.dout, mode=self.mode,
+                          scale=self.scale, dq=self.grads[0], dk=self.grads[1], dv=self.grads[2],
+                          workspace=self.ws)
+
+    def summary(self, world, steps, max_over_ranks, dev, peak, src):
+        B, H, T, d = self.shape
+        pairs = B * H * T * (T + 3) // 2
+        flops = 10 * d * pairs  # S, dP, dV, dK, dQ: 2 d flops each per (query, key) pair
+        tot = max_over_ranks(sum(self.ms), device=dev)
+        ms = tot / steps
+        achieved = flops / (ms * 1e-3) / 1e12
+        return {
+            "metric": f"continuous-attn bwd TFLOP/s (B={B},H={H},T={T},d={d}, bf16, causal)",
+            "value": round(world * achieved, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
+            "steps": steps,
+            "flops_per_step": flops,
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                         "peak_source": f"{src} bf16 dense (burst)", "traffic": None,
+                         "timed": "whole csa_backward call (D row dot, tensor-core kernel, dq "
+                                  "conversion)"},
+            "gpu_launches_per_step": self.launches,
+        }
 
 
 class DecodeBench:
@@ -486,6 +543,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=256, help="oracle rows per reference step")
     ap.add_argument("--decode-steps", type=int, default=200, help="timed steps of the decode workload")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode workload")
+    ap.add_argument("--backward-steps", type=int, default=50, help="timed steps of the backward pass")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward pass")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -113,7 +113,9 @@ int decode_bf16(const void *q, const void *k_cache, const void *v_cache, const v
 
 long long backward_scratch_bytes(int B, int H, int T, int d) {
     if (B < 0 || H < 0 || T < 0 || d < 1 || d > 256) return -1;
-    return csa_simt_backward_scratch_bytes(B, H, T, d);
+    const long long a = csa_simt_backward_scratch_bytes(B, H, T, d);
+    const long long b = csa_tc_backward_scratch_bytes(B, H, T, d);
+    return a > b ? a : b;
 }
 
 int backward_any(const void *q, const void *k, const void *v, const void *k0, const void *v0,
@@ -151,6 +153,13 @@ int backward_any(const void *q, const void *k, const void *v, const void *k0, co
         return CSA_ERR_ALIGNMENT;
     if ((rc = device_ok()) != CSA_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool tc_aligned = aligned(q, 16) && aligned(k, 16) && aligned(v, 16) &&
+                            aligned(out, 16) && aligned(dout, 16) && aligned(dq, 16) &&
+                            aligned(dk, 16) && aligned(dv, 16) &&
+                            (mode != CSA_K0_GIVEN || (aligned(k0, 16) && aligned(v0, 16)));
+    if (bf16 && (d == 64 || d == 128) && tc_aligned)
+        return csa_tc_backward(q, k, v, k0, v0, out, lse, dout, dq, dk, dv, dk0, dv0, workspace,
+                               B, H, T, d, scale, mode, s);
     if (bf16)
         return from_cuda(csa_simt_backward_bf16(q, k, v, k0, v0, out, lse, dout, dq, dk, dv, dk0,
                                                 dv0, workspace, B, H, T, d, scale, mode, s));
@@ -249,7 +258,8 @@ int csa_device_status(void) {
     const int a = csa_tc_take_status();
     const int b = csa_tc_std_take_status();
     const int c = csa_decode_take_status();
-    return a != CSA_OK ? a : b != CSA_OK ? b : c;
+    const int e = csa_tc_backward_take_status();
+    return a != CSA_OK ? a : b != CSA_OK ? b : c != CSA_OK ? c : e;
 }
 
 int csa_selftest_wait_timeout(unsigned timeout_us, csa_stream_t stream) {

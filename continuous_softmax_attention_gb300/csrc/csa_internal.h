@@ -56,3 +56,14 @@ cudaError_t csa_simt_backward_bf16(const void *q, const void *k, const void *v, 
                                    const void *dout, void *dq, void *dk, void *dv, float *dk0,
                                    float *dv0, void *scratch, int B, int H, int T, int d,
                                    float scale, int mode, cudaStream_t stream);
+
+// Backward pass on the tensor cores (csa_tc_bwd.cu), bf16, d in {64, 128},
+// all tensors 16-byte aligned.  scratch: csa_tc_backward_scratch_bytes bytes
+// (fp32 dq accumulator and the per-row D = dout . out).  Returns a CSA_*
+// status code.
+long long csa_tc_backward_scratch_bytes(int B, int H, int T, int d);
+int csa_tc_backward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+                    const void *o, const float *lse, const void *dout, void *dq, void *dk,
+                    void *dv, float *dk0, float *dv0, void *scratch, int B, int H, int T, int d,
+                    float scale, int mode, cudaStream_t stream);
+int csa_tc_backward_take_status(void);

@@ -1,0 +1,645 @@
+// Tensor-core backward kernel of causal continuous attention for sm_103a:
+// the gradient of eq. (10)/(11) of Jianlin Su, "Continuous Softmax
+// Attention" ("Assembly and Simplification"), bf16 inputs, d = 64 or 128.
+//
+// With p_i = e^{a_i - lse} (a_i = scale q.k_i), the interval between keys
+// c and c+1 (natural step x) hands key c the share R = p_c phi2(x) and key
+// c+1 the share L = p_{c+1} phi2(-x) of eq. (9), so P_c = L_c + R_c.  Their
+// derivatives with respect to the two end logits combine, for each row, to
+//     dL/da_c = P_c (dP_c - D) + F_c - F_{c+1},  F_c = k_c (dP_{c-1} - dP_c),
+// where k_c = p_{c-1} phi2'(x) is the interval's flux coefficient,
+// dP = dO . v and D = dO . o.  dS = scale dL/da, and
+//     dV = P^T dO,  dK = dS^T Q,  dQ = dS K.
+//
+// Work split.  One CTA owns one key tile of one (b, h): 128 consecutive keys
+// of the extended sequence (the sink first) at a stride of 126, so that its
+// columns 1..126 are its own keys and columns 0 and 127 are the neighbours
+// the stencil needs (for key tile 0, column 0 is the sink itself).  The CTA
+// walks the 128-row query tiles from its diagonal to the end.  Per query
+// tile the tensor core forms S = Q K^T and dP = dO V^T in TMEM; eight
+// warps turn them into P and dS (bf16), written once to shared memory in the
+// 128B-swizzled layout that serves as the MN-major A operand of
+// dV += P^T dO and dK += dS^T Q and as the K-major A operand of
+// dQ_part = dS K.  dV and dK accumulate in TMEM over the whole walk; dQ_part
+// goes to TMEM (in the S columns) and is added to an fp32 dq accumulator in
+// global memory with vector reductions.  Warps:
+//   0-7  elementwise: warp w owns TMEM lanes 32*(w%4).. and the column half
+//        w/4 (64 columns); they also run the dQ and final dK/dV epilogues
+//   8    TMA producer (the key tile once, then Q and dO per query tile)
+//   9    TMEM allocator and tcgen05.mma issuer
+// Tensor memory: S (then dQ_part) | dP | dV | dK.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "csa.h"
+#include "csa_internal.h"
+#include "csa_tc_common.cuh"
+
+using namespace csa_tc;
+
+namespace {
+
+__device__ int g_bwd_status;  // sticky status word of this file's kernels
+
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+constexpr int kThreads = 32 * 10;
+constexpr int kKeyStride = 126;  // owned keys per key tile
+
+// tcgen05.mma kind::f16 instruction descriptor with the major-ness of A and
+// B chosen separately (fp32 accumulator, bf16 A and B).
+__host__ __device__ constexpr uint32_t idesc_ab(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// tcgen05.wait::ld naming the 17 registers it waits for, so that no use of
+// them is scheduled before it.
+__device__ __forceinline__ void wait_ld17(uint32_t (&r)[16], uint32_t &x) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(x)
+                 :
+                 : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+template <int D>
+struct BwCfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kTileBytes = kChunks * kChunkBytes;  // [128 rows][D] bf16
+    static constexpr int kStages = D == 128 ? 1 : 2;          // Q + dO stages
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kTileBytes;
+    static constexpr int kOffQ = kOffV + kTileBytes;             // [stage]
+    static constexpr int kOffG = kOffQ + kStages * kTileBytes;   // [stage] dO
+    static constexpr int kOffP = kOffG + kStages * kTileBytes;   // 2 boxes [128 q][64 keys]
+    static constexpr int kOffS = kOffP + 2 * kChunkBytes;        // dS, same layout
+    static constexpr int kOffBar = kOffS + 2 * kChunkBytes;
+    static constexpr int kBarKV = 0;
+    static constexpr int kBarQFull = 1;
+    static constexpr int kBarQEmpty = kBarQFull + kStages;
+    static constexpr int kBarSFull = kBarQEmpty + kStages;  // S and dP in TMEM
+    static constexpr int kBarPReady = kBarSFull + 1;        // P, dS in shared memory
+    static constexpr int kBarDqFull = kBarPReady + 1;       // dV, dK, dQ_part MMAs done
+    static constexpr int kBarDqRead = kBarDqFull + 1;       // dQ_part read out of TMEM
+    static constexpr int kBarDrain = kBarDqRead + 1;
+    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
+    static constexpr uint32_t kColS = 0;
+    static constexpr uint32_t kColP = 128;
+    static constexpr uint32_t kColV = 256;
+    static constexpr uint32_t kColK = 256 + D;
+};
+
+struct BwParams {
+    int B, H, T;
+    int nq, nk;  // query tiles (128 rows), key tiles (126 keys)
+    int group;   // heads per scheduling group
+    float scale, k2;  // scale, scale * log2(e)
+    int mode;
+    const __nv_bfloat16 *k0, *v0;
+    const float *lse, *Drow;  // [B*H*T]
+    float *dq_acc;            // [B*H*T*D]
+    __nv_bfloat16 *dk, *dv;
+    float *dk0, *dv0;
+};
+
+__device__ __forceinline__ bool wait_b(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    return wait_bar(bar, parity, abort_flag, &g_bwd_status);
+}
+
+// One interval between a left key at u0 and a right key at u1 (log2 units,
+// u = a log2(e) - lse log2(e), p = 2^u): R = p0 phi2(x), L = p1 phi2(-x)
+// and the flux coefficient k = p0 phi2'(x), x = (u1 - u0) ln 2.
+// Closed forms through the interval integral s = (p1 - p0)/x = p0 phi1(x):
+//     R = (s - p0)/x,  L = s - R,  k = (s - 2R)/x,
+// using phi2' = (phi1 - 2 phi2)/x and identity (7).  The independent
+// rounding of p0 and p1 grows by up to 24/x^3 in k, so |x| < 1/2 takes the
+// power series of the integral definitions instead (degree 5, truncation
+// below 3e-6):  phi2 = sum x^n/(n+2)!,  phi1 - phi2 = sum (n+1) x^n/(n+2)!,
+// phi2' = sum (n+1) x^n/(n+3)!, all times p0.
+__device__ __forceinline__ void interval(float u0, float u1, float p0, float p1, float &R,
+                                         float &L, float &k) {
+    const float x = (u1 - u0) * kLn2;
+    float f2 = 1.0f / 5040.0f, f12 = 1.0f / 840.0f, f3 = 1.0f / 6720.0f;
+    f2 = fmaf(f2, x, 1.0f / 720.0f);
+    f12 = fmaf(f12, x, 1.0f / 144.0f);
+    f3 = fmaf(f3, x, 1.0f / 1008.0f);
+    f2 = fmaf(f2, x, 1.0f / 120.0f);
+    f12 = fmaf(f12, x, 1.0f / 30.0f);
+    f3 = fmaf(f3, x, 1.0f / 180.0f);
+    f2 = fmaf(f2, x, 1.0f / 24.0f);
+    f12 = fmaf(f12, x, 1.0f / 8.0f);
+    f3 = fmaf(f3, x, 1.0f / 40.0f);
+    f2 = fmaf(f2, x, 1.0f / 6.0f);
+    f12 = fmaf(f12, x, 1.0f / 3.0f);
+    f3 = fmaf(f3, x, 1.0f / 12.0f);
+    f2 = fmaf(f2, x, 0.5f);
+    f12 = fmaf(f12, x, 0.5f);
+    f3 = fmaf(f3, x, 1.0f / 6.0f);
+    const float rx = rcp_approx(x);
+    const float s = (p1 - p0) * rx;
+    const float Rc = (s - p0) * rx;
+    const float kc = fmaf(-2.0f, Rc, s) * rx;
+    const bool small = fabsf(x) < 0.5f;
+    R = small ? p0 * f2 : Rc;
+    L = small ? p0 * f12 : s - Rc;
+    k = small ? p0 * f3 : kc;
+}
+
+// 16 columns [c0, c0+16) of this row: P and dS, given the raw logits sv[]
+// and dP values gv[] of columns c0..c0+16 (the last one the right
+// neighbour), the row's lse (log2 units) and D, and the L share and flux of
+// column c0 from its left interval (Lc, Fc; updated to those of c0+16).
+// Column c is a key of this row iff c <= c_last; the interval (c, c+1)
+// exists iff c + 1 <= c_last and c + 1 <= 127.
+__device__ __forceinline__ void cols16(const float (&sv)[17], const float (&gv)[17], float k2,
+                                       float lse2, float Dr, float scale, int c0, int c_last,
+                                       bool zero_c0, float &Lc, float &Fc, uint32_t (&pP)[8],
+                                       uint32_t (&pS)[8]) {
+    float u[17], pe[17];
+#pragma unroll
+    for (int i = 0; i < 17; ++i) {
+        u[i] = fmaf(sv[i], k2, -lse2);
+        pe[i] = ex2_approx(u[i]);
+    }
+    float Pv[16], Sv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int c = c0 + i;
+        float R, Ln, kf;
+        interval(u[i], u[i + 1], pe[i], pe[i + 1], R, Ln, kf);
+        const bool seg = c + 1 <= c_last && c + 1 <= 127;
+        R = seg ? R : 0.0f;
+        Ln = seg ? Ln : 0.0f;
+        const float Fn = seg ? kf * (gv[i] - gv[i + 1]) : 0.0f;
+        const bool key = c <= c_last;
+        const float P = key ? Lc + R : 0.0f;
+        float ds = key ? scale * fmaf(P, gv[i] - Dr, Fc - Fn) : 0.0f;
+        // columns that belong to the neighbouring key tiles take no part in dQ
+        if (c == 127 || (c == 0 && zero_c0)) ds = 0.0f;
+        Pv[i] = P;
+        Sv[i] = ds;
+        Lc = Ln;
+        Fc = Fn;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        pP[i] = pack_bf16x2(Pv[2 * i], Pv[2 * i + 1]);
+        pS[i] = pack_bf16x2(Sv[2 * i], Sv[2 * i + 1]);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_backward_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_g, const BwParams p) {
+    using C = BwCfg<D>;
+    constexpr int NS = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    const uint32_t sK = base + C::kOffK, sV = base + C::kOffV, sQ = base + C::kOffQ;
+    const uint32_t sG = base + C::kOffG, sP = base + C::kOffP, sS = base + C::kOffS;
+    const uint32_t bars = base + C::kOffBar;
+#define BAR(i) (bars + 8u * (uint32_t)(i))
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Heads in groups whose Q and dO fit in L2 together; within a group the
+    // longest walks (the first key tiles) go first.
+    const int nk = p.nk, BH = p.B * p.H;
+    const int grp = (int)(blockIdx.x / (unsigned)(p.group * nk));
+    const int gsz = min(p.group, BH - grp * p.group);
+    const int idx = (int)blockIdx.x - grp * p.group * nk;
+    const int bh = grp * p.group + idx % gsz;
+    const int kt = idx / gsz;
+    const int T = p.T;
+    const int krow0 = kKeyStride * kt - 1;          // array row of tile column 0
+    const int q_first = (kKeyStride * kt) / 128;    // first query tile that sees an owned key
+    const int nQ = p.nq - q_first;
+
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(C::kBarKV), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(BAR(C::kBarQFull + s), 1);
+            mbar_init(BAR(C::kBarQEmpty + s), 1);
+        }
+        mbar_init(BAR(C::kBarSFull), 1);
+        mbar_init(BAR(C::kBarPReady), 256);
+        mbar_init(BAR(C::kBarDqFull), 1);
+        mbar_init(BAR(C::kBarDqRead), 256);
+        mbar_init(BAR(C::kBarDrain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kWarpProducer) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_g);
+            mbar_arrive_expect_tx(BAR(C::kBarKV), 2 * C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c) {
+                tma_load_3d(sK + c * kChunkBytes, &tm_k, 64 * c, krow0, bh, BAR(C::kBarKV));
+                tma_load_3d(sV + c * kChunkBytes, &tm_v, 64 * c, krow0, bh, BAR(C::kBarKV));
+            }
+            int issued = 0;
+            for (int j = 0; j < nQ; ++j) {
+                const int s = j % NS;
+                if (!wait_b(BAR(C::kBarQEmpty + s), ((j / NS) & 1) ^ 1, abort_flag)) break;
+                const int qrow = 128 * (q_first + j);
+                mbar_arrive_expect_tx(BAR(C::kBarQFull + s), 2 * C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d(sQ + s * C::kTileBytes + c * kChunkBytes, &tm_q, 64 * c, qrow, bh,
+                                BAR(C::kBarQFull + s));
+                    tma_load_3d(sG + s * C::kTileBytes + c * kChunkBytes, &tm_g, 64 * c, qrow, bh,
+                                BAR(C::kBarQFull + s));
+                }
+                issued = j + 1;
+            }
+            // Let every copy this thread issued land before the block can exit.
+            wait_bar_drain(BAR(C::kBarKV), 0, &g_bwd_status);
+            for (int j = max(0, issued - NS); j < issued; ++j)
+                wait_bar_drain(BAR(C::kBarQFull + j % NS), (j / NS) & 1, &g_bwd_status);
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc_ab(128, 128, false, false);  // S, dP
+            constexpr uint32_t kIdKV = idesc_ab(128, D, true, true);     // dV, dK
+            constexpr uint32_t kIdQ = idesc_ab(128, D, false, true);     // dQ_part
+            bool ok = wait_b(BAR(C::kBarKV), 0, abort_flag);
+            if (ok && kt == 0 && p.mode != 0) {
+                // The sink is column 0 of key tile 0 (array row -1, read as
+                // zeros): the copy-first mode takes key 1's row, the given
+                // mode k0[h] and v0[h].  Rows r of a 128B-swizzled box keep
+                // their 16-byte chunk c at position c ^ (r & 7).
+                const size_t hoff = (size_t)(bh % p.H) * D;
+                for (int c = 0; c < D / 8; ++c) {
+                    uint8_t *k_row0 = smem + C::kOffK + (c >> 3) * kChunkBytes + ((c & 7) << 4);
+                    uint8_t *v_row0 = smem + C::kOffV + (c >> 3) * kChunkBytes + ((c & 7) << 4);
+                    uint4 kv, vv;
+                    if (p.mode == 1) {
+                        const int pos1 = ((c & 7) ^ 1) << 4;  // row 1
+                        kv = *reinterpret_cast<const uint4 *>(smem + C::kOffK + (c >> 3) * kChunkBytes + 128 + pos1);
+                        vv = *reinterpret_cast<const uint4 *>(smem + C::kOffV + (c >> 3) * kChunkBytes + 128 + pos1);
+                    } else {
+                        kv = *reinterpret_cast<const uint4 *>(p.k0 + hoff + 8 * c);
+                        vv = *reinterpret_cast<const uint4 *>(p.v0 + hoff + 8 * c);
+                    }
+                    *reinterpret_cast<uint4 *>(k_row0) = kv;
+                    *reinterpret_cast<uint4 *>(v_row0) = vv;
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_after();
+            for (int j = 0; ok && j < nQ; ++j) {
+                const int s = j % NS;
+                const uint32_t qb = sQ + s * C::kTileBytes, gb = sG + s * C::kTileBytes;
+                if (!(ok = wait_b(BAR(C::kBarQFull + s), (j / NS) & 1, abort_flag))) break;
+                // S overwrites the dQ_part columns of the previous tile
+                if (j > 0 && !(ok = wait_b(BAR(C::kBarDqRead), (j - 1) & 1, abort_flag))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    tc_mma_ss(tmem + C::kColS, make_sdesc(qb + off, 16, 1024),
+                              make_sdesc(sK + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    tc_mma_ss(tmem + C::kColP, make_sdesc(gb + off, 16, 1024),
+                              make_sdesc(sV + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(BAR(C::kBarSFull));
+                if (!(ok = wait_b(BAR(C::kBarPReady), j & 1, abort_flag))) break;
+                tc_fence_after();
+                // dV += P^T dO and dK += dS^T Q: A = P^T / dS^T, MN-major (keys
+                // contiguous, two 64-key boxes); B = dO / Q, MN-major; the
+                // reduction runs over the 128 query rows, 16 per step.
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                    tc_mma_ss(tmem + C::kColV, make_sdesc(sP + kk * 2048, kChunkBytes, 1024),
+                              make_sdesc(gb + kk * 2048, kChunkBytes, 1024), kIdKV, acc);
+                    tc_mma_ss(tmem + C::kColK, make_sdesc(sS + kk * 2048, kChunkBytes, 1024),
+                              make_sdesc(qb + kk * 2048, kChunkBytes, 1024), kIdKV, acc);
+                }
+                // dQ_part = dS K: A = dS K-major (reduction over the 128 keys),
+                // B = the key tile, MN-major
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    tc_mma_ss(tmem + C::kColS, make_sdesc(sS + off, 16, 1024),
+                              make_sdesc(sK + kk * 2048, kChunkBytes, 1024), kIdQ, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(BAR(C::kBarDqFull));
+                tc_commit(BAR(C::kBarQEmpty + s));
+            }
+            // every MMA this thread issued completes before the block exits
+            tc_commit(BAR(C::kBarDrain));
+            wait_bar_drain(BAR(C::kBarDrain), 0, &g_bwd_status);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------ elementwise
+        const int half = warp >> 2, wq = warp & 3;
+        const int irow = wq * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + C::kColS, tD = tmem + lane_off + C::kColP;
+        const float k2 = p.k2, scale = p.scale;
+        bool ok = true;
+        for (int j = 0; ok && j < nQ; ++j) {
+            const int r = 128 * (q_first + j) + irow;  // query row
+            const bool rvalid = r < T;
+            const float lse2 = rvalid ? p.lse[(size_t)bh * T + r] * kLog2e : 0.0f;
+            const float Dr = rvalid ? p.Drow[(size_t)bh * T + r] : 0.0f;
+            // last column of the tile this row sees (its own key, position r + 1)
+            const int c_last = rvalid ? min(r + 1 - kKeyStride * kt, 127) : -1;
+            ok = __all_sync(0xffffffffu, wait_b(BAR(C::kBarSFull), j & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            // L share and flux entering this half's first column from the left
+            float Lc = 0.0f, Fc = 0.0f;
+            if (half == 1) {
+                uint32_t e[4];
+                tmem_ld1(tS + 63, e[0]);
+                tmem_ld1(tS + 64, e[1]);
+                tmem_ld1(tD + 63, e[2]);
+                tmem_ld1(tD + 64, e[3]);
+                asm volatile("tcgen05.wait::ld.sync.aligned;"
+                             : "+r"(e[0]), "+r"(e[1]), "+r"(e[2]), "+r"(e[3])
+                             :
+                             : "memory");
+                const float u0 = fmaf(__uint_as_float(e[0]), k2, -lse2);
+                const float u1 = fmaf(__uint_as_float(e[1]), k2, -lse2);
+                float R, L, kf;
+                interval(u0, u1, ex2_approx(u0), ex2_approx(u1), R, L, kf);
+                const bool seg = 64 <= c_last;
+                Lc = seg ? L : 0.0f;
+                Fc = seg ? kf * (__uint_as_float(e[2]) - __uint_as_float(e[3])) : 0.0f;
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const int c0 = 64 * half + 16 * kk;
+                uint32_t a[16], g[16], an[1] = {0u}, gn[1] = {0u};
+                tmem_ld16(tS + c0, a);
+                tmem_ld16(tD + c0, g);
+                if (c0 + 16 <= 127) {
+                    tmem_ld1(tS + c0 + 16, an[0]);
+                    tmem_ld1(tD + c0 + 16, gn[0]);
+                }
+                wait_ld17(a, an[0]);
+                wait_ld17(g, gn[0]);  // already complete: only ties g, gn to the wait
+                float sv[17], gv[17];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    sv[i] = __uint_as_float(a[i]);
+                    gv[i] = __uint_as_float(g[i]);
+                }
+                sv[16] = __uint_as_float(an[0]);
+                gv[16] = __uint_as_float(gn[0]);
+                uint32_t pP[8], pS[8];
+                cols16(sv, gv, k2, lse2, Dr, scale, c0, c_last, kt > 0, Lc, Fc, pP, pS);
+                // this row's 16 keys = 16-byte chunks 2*(c0%64)/16 .. +1 of box c0/64
+                const int box = c0 >> 6, ch = (c0 & 63) >> 3;
+                uint8_t *prow = smem + C::kOffP + box * kChunkBytes + irow * 128;
+                uint8_t *srow = smem + C::kOffS + box * kChunkBytes + irow * 128;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int pos = ((ch + h2) ^ (irow & 7)) << 4;
+                    *reinterpret_cast<uint4 *>(prow + pos) =
+                        make_uint4(pP[4 * h2], pP[4 * h2 + 1], pP[4 * h2 + 2], pP[4 * h2 + 3]);
+                    *reinterpret_cast<uint4 *>(srow + pos) =
+                        make_uint4(pS[4 * h2], pS[4 * h2 + 1], pS[4 * h2 + 2], pS[4 * h2 + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(BAR(C::kBarPReady));
+            // dQ_part of this query tile, added into the fp32 accumulator
+            ok = __all_sync(0xffffffffu, wait_b(BAR(C::kBarDqFull), j & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            float *dst = p.dq_acc + ((size_t)bh * T + (size_t)(rvalid ? r : 0)) * D + half * (D / 2);
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
+                uint32_t o[32];
+                tmem_ld32(tS + half * (D / 2) + 32 * cc, o);
+                tmem_wait_ld_regs<32>(o);
+                if (rvalid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        red_add_v4(dst + 32 * cc + e, __uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                   __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(BAR(C::kBarDqRead));
+        }
+        if (ok) {
+            // dV, dK of this tile's keys: TMEM lane = key row of the tile.
+            // The last DqFull wait covers every MMA of the walk.
+            const int c = irow;
+            const int arow = krow0 + c;
+            const bool own = c >= 1 && c <= kKeyStride && arow < T;
+            const int h = bh % p.H;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t tcol = tmem + lane_off + (which ? C::kColK : C::kColV) + half * (D / 2);
+                __nv_bfloat16 *outp = which ? p.dk : p.dv;
+                float *sinkp = which ? p.dk0 : p.dv0;
+#pragma unroll
+                for (int cc = 0; cc < D / 64; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(tcol + 32 * cc, o);
+                    tmem_wait_ld_regs<32>(o);
+                    float val[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) val[e] = __uint_as_float(o[e]);
+                    const int col0 = half * (D / 2) + 32 * cc;
+                    if (kt == 0 && wq == 0) {
+                        // the sink (row 0): its own gradient, or key 1's share
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float sinkv = __shfl_sync(0xffffffffu, val[e], 0);
+                            if (p.mode == 1 && c == 1) val[e] += sinkv;
+                        }
+                        if (p.mode == 2 && c == 0) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) atomicAdd(sinkp + (size_t)h * D + col0 + e, val[e]);
+                        }
+                    }
+                    if (own) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(val[2 * e], val[2 * e + 1]);
+                        uint4 *dstp = reinterpret_cast<uint4 *>(outp + ((size_t)bh * T + arow) * D + col0);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dstp[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+#undef BAR
+}
+
+// D_t = dO_t . o_t for every row (one warp per row), and dq (bf16) from its
+// fp32 accumulator.
+template <int D>
+__global__ void row_dot_kernel(const __nv_bfloat16 *g, const __nv_bfloat16 *o, float *Drow,
+                               long long rows) {
+    const long long w = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (w >= rows) return;
+    const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(g + w * D);
+    const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(o + w * D);
+    float s = 0.0f;
+#pragma unroll
+    for (int i = lane; i < D / 2; i += 32) {
+        const float2 a = __bfloat1622float2(g2[i]), b = __bfloat1622float2(o2[i]);
+        s = fmaf(a.x, b.x, fmaf(a.y, b.y, s));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) Drow[w] = s;
+}
+
+__global__ void to_bf16_kernel(const float *a, __nv_bfloat16 *out, long long n4) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n4) return;
+    const float4 v = reinterpret_cast<const float4 *>(a)[i];
+    uint2 pk;
+    pk.x = pack_bf16x2(v.x, v.y);
+    pk.y = pack_bf16x2(v.z, v.w);
+    reinterpret_cast<uint2 *>(out)[i] = pk;
+}
+
+template <int D>
+int launch_bwd(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+               const void *o, const float *lse, const void *dout, void *dq, void *dk, void *dv,
+               float *dk0, float *dv0, void *scratch, int B, int H, int T, float scale, int mode,
+               cudaStream_t stream) {
+    using C = BwCfg<D>;
+    const int BH = B * H;
+    const long long rows = (long long)BH * T;
+    float *dq_acc = static_cast<float *>(scratch);
+    float *Drow = dq_acc + rows * D;
+    CUtensorMap mq, mk, mv, mg;
+    if (!encode_qkv_map(&mq, q, BH, T, D) || !encode_qkv_map(&mk, k, BH, T, D) ||
+        !encode_qkv_map(&mv, v, BH, T, D) || !encode_qkv_map(&mg, dout, BH, T, D))
+        return CSA_ERR_CUDA;
+    if (cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)rows * D, stream) != cudaSuccess)
+        return CSA_ERR_CUDA;
+    if (mode == 2 && (cudaMemsetAsync(dk0, 0, sizeof(float) * (size_t)H * D, stream) != cudaSuccess ||
+                      cudaMemsetAsync(dv0, 0, sizeof(float) * (size_t)H * D, stream) != cudaSuccess))
+        return CSA_ERR_CUDA;
+    row_dot_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(dout), static_cast<const __nv_bfloat16 *>(o), Drow, rows);
+    BwParams prm;
+    prm.B = B;
+    prm.H = H;
+    prm.T = T;
+    prm.nq = (T + 127) / 128;
+    prm.nk = (T + kKeyStride - 1) / kKeyStride;
+    // Q and dO of a head are read by all of its key tiles: as many heads per
+    // group as keep those within 64 MiB.
+    prm.group = heads_per_group(BH, T, D);
+    prm.scale = scale;
+    prm.k2 = scale * kLog2e;
+    prm.mode = mode;
+    prm.k0 = static_cast<const __nv_bfloat16 *>(k0);
+    prm.v0 = static_cast<const __nv_bfloat16 *>(v0);
+    prm.lse = lse;
+    prm.Drow = Drow;
+    prm.dq_acc = dq_acc;
+    prm.dk = static_cast<__nv_bfloat16 *>(dk);
+    prm.dv = static_cast<__nv_bfloat16 *>(dv);
+    prm.dk0 = dk0;
+    prm.dv0 = dv0;
+    const long long grid = (long long)prm.nk * BH;
+    if (grid > 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
+    auto kern = tc_backward_kernel<D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+        return CSA_ERR_CUDA;
+    kern<<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mg, prm);
+    const long long n4 = rows * D / 4;
+    to_bf16_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, stream>>>(
+        dq_acc, static_cast<__nv_bfloat16 *>(dq), n4);
+    return cudaGetLastError() == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+}
+
+}  // namespace
+
+long long csa_tc_backward_scratch_bytes(int B, int H, int T, int d) {
+    return (long long)B * H * T * ((long long)d + 1) * (long long)sizeof(float);
+}
+
+int csa_tc_backward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+                    const void *o, const float *lse, const void *dout, void *dq, void *dk,
+                    void *dv, float *dk0, float *dv0, void *scratch, int B, int H, int T, int d,
+                    float scale, int mode, cudaStream_t stream) {
+    if (d == 128)
+        return launch_bwd<128>(q, k, v, k0, v0, o, lse, dout, dq, dk, dv, dk0, dv0, scratch, B, H,
+                               T, scale, mode, stream);
+    if (d == 64)
+        return launch_bwd<64>(q, k, v, k0, v0, o, lse, dout, dq, dk, dv, dk0, dv0, scratch, B, H, T,
+                              scale, mode, stream);
+    return CSA_ERR_UNSUPPORTED;
+}
+
+int csa_tc_backward_take_status(void) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_bwd_status, sizeof(int)) != cudaSuccess) return CSA_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(int)) != cudaSuccess) return CSA_ERR_CUDA;
+    return v;
+}

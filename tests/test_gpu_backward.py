@@ -109,3 +109,50 @@ def test_backward_empty_and_errors():
         backward(dev["q"], dev["k"], dev["v"], o, lse, dev["q"], workspace=small)
     assert err.value.code == -1
     assert backward_workspace_bytes(1, 2, 8, 16) >= 2 * 8 * 16 * 4 * 2
+
+
+@pytest.mark.parametrize("d,mode,T", [(128, 0, 700), (64, 2, 700), (128, 1, 383), (64, 0, 1000)])
+def test_backward_tensor_core_tiles(d, mode, T):
+    """Several key tiles (126 keys each, halo columns on both sides) and query
+    tiles (128 rows), a ragged last tile, rows at every tile edge."""
+    x = make_inputs(1, 2, T, d, "bf16", seed=160 + T + mode)
+    g = upstream((1, 2, T, d), 10)
+    compare(x, g, 1.0 / d ** 0.5, mode, "bf16", f"tc d={d} mode={mode} T={T}")
+
+
+@pytest.mark.parametrize("scale", [0.02, 0.35])
+def test_backward_tensor_core_logit_ranges(scale):
+    # scale 0.35 at d = 64: logit gaps of several units between neighbours
+    x = make_inputs(2, 2, 300, 64, "bf16", seed=170)
+    g = upstream((2, 2, 300, 64), 11)
+    compare(x, g, scale, 0, "bf16", f"tc scale={scale}")
+
+
+def test_backward_tensor_core_matches_cuda_core_path():
+    """Tensors offset by one element (2-byte aligned only) take the CUDA-core
+    path; the default 16-byte aligned ones the tensor-core path.  Both are
+    held to the oracle's bar here, and they must agree with each other."""
+    B, H, T, d = 1, 2, 260, 64
+    x = make_inputs(B, H, T, d, "bf16", seed=180)
+    g = upstream((B, H, T, d), 12).to(torch.bfloat16)
+    dev = {k: t.cuda() for k, t in x.items()}
+    o, lse = forward(dev["q"], dev["k"], dev["v"], mode=0)
+    gd = g.cuda()
+    tc = backward(dev["q"], dev["k"], dev["v"], o, lse, gd, mode=0)
+
+    def off(t):  # same values, data pointer 2 bytes past a 16-byte boundary
+        buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=t.device)
+        v = buf[1:1 + t.numel()].view(t.shape)
+        v.copy_(t)
+        return v
+
+    outs = [off(torch.empty_like(dev["q"])) for _ in range(3)]
+    simt = backward(off(dev["q"]), off(dev["k"]), off(dev["v"]), off(o), lse, off(gd), mode=0,
+                    dq=outs[0], dk=outs[1], dv=outs[2])
+    torch.cuda.synchronize()
+    ref = oracle.backward(x["q"], x["k"], x["v"], g.float(), scale=1.0 / d ** 0.5, mode=0)
+    for name, a, b in zip(("dq", "dk", "dv"), tc[:3], simt[:3]):
+        check(a, ref[name], "bf16", "tensor-core " + name)
+        check(b, ref[name], "bf16", "cuda-core " + name)
+        diff = (a.float() - b.float()).abs().max().item()
+        assert diff <= 2e-2 * np.abs(ref[name]).max(), (name, diff)
