@@ -21,13 +21,14 @@
 // 128B-swizzled layout that serves as the MN-major A operand of
 // dV += P^T dO and dK += dS^T Q and as the K-major A operand of
 // dQ_part = dS K.  dV and dK accumulate in TMEM over the whole walk; dQ_part
-// goes to TMEM (in the S columns) and is added to an fp32 dq accumulator in
-// global memory with vector reductions.  Warps:
+// goes to TMEM (in the dP columns, so that the next S product need not wait
+// for it to be read) and is added to an fp32 dq accumulator in global
+// memory with vector reductions.  Warps:
 //   0-7  elementwise: warp w owns TMEM lanes 32*(w%4).. and the column half
 //        w/4 (64 columns); they also run the dQ and final dK/dV epilogues
 //   8    TMA producer (the key tile once, then Q and dO per query tile)
 //   9    TMEM allocator and tcgen05.mma issuer
-// Tensor memory: S (then dQ_part) | dP | dV | dK.
+// Tensor memory: S | dP (then dQ_part) | dV | dK.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -137,20 +138,16 @@ __device__ __forceinline__ bool wait_b(uint32_t bar, uint32_t parity, volatile i
 // Closed forms through the interval integral s = (p1 - p0)/x = p0 phi1(x):
 //     R = (s - p0)/x,  L = s - R,  k = (s - 2R)/x,
 // using phi2' = (phi1 - 2 phi2)/x and identity (7).  The independent
-// rounding of p0 and p1 grows by up to 24/x^3 in k, so |x| < 1/2 takes the
-// power series of the integral definitions instead (degree 5, truncation
-// below 3e-6):  phi2 = sum x^n/(n+2)!,  phi1 - phi2 = sum (n+1) x^n/(n+2)!,
-// phi2' = sum (n+1) x^n/(n+3)!, all times p0.
+// rounding of p0 and p1 (2^-22 each) grows by up to 24/|x|^3 in k, so
+// |x| < 0.35 takes the power series of the integral definitions instead,
+//     phi2 = sum x^n/(n+2)!,  phi1 - phi2 = sum (n+1) x^n/(n+2)!,
+//     phi2' = sum (n+1) x^n/(n+3)!,
+// to degree 3, all times p0.  Both sides of the switch stay below 3e-4
+// relative error, under the 2^-9 rounding of the bf16 P and dS.
 __device__ __forceinline__ void interval(float u0, float u1, float p0, float p1, float &R,
                                          float &L, float &k) {
     const float x = (u1 - u0) * kLn2;
-    float f2 = 1.0f / 5040.0f, f12 = 1.0f / 840.0f, f3 = 1.0f / 6720.0f;
-    f2 = fmaf(f2, x, 1.0f / 720.0f);
-    f12 = fmaf(f12, x, 1.0f / 144.0f);
-    f3 = fmaf(f3, x, 1.0f / 1008.0f);
-    f2 = fmaf(f2, x, 1.0f / 120.0f);
-    f12 = fmaf(f12, x, 1.0f / 30.0f);
-    f3 = fmaf(f3, x, 1.0f / 180.0f);
+    float f2 = 1.0f / 120.0f, f12 = 1.0f / 30.0f, f3 = 1.0f / 180.0f;
     f2 = fmaf(f2, x, 1.0f / 24.0f);
     f12 = fmaf(f12, x, 1.0f / 8.0f);
     f3 = fmaf(f3, x, 1.0f / 40.0f);
@@ -164,7 +161,7 @@ __device__ __forceinline__ void interval(float u0, float u1, float p0, float p1,
     const float s = (p1 - p0) * rx;
     const float Rc = (s - p0) * rx;
     const float kc = fmaf(-2.0f, Rc, s) * rx;
-    const bool small = fabsf(x) < 0.5f;
+    const bool small = fabsf(x) < 0.35f;
     R = small ? p0 * f2 : Rc;
     L = small ? p0 * f12 : s - Rc;
     k = small ? p0 * f3 : kc;
@@ -174,12 +171,16 @@ __device__ __forceinline__ void interval(float u0, float u1, float p0, float p1,
 // and dP values gv[] of columns c0..c0+16 (the last one the right
 // neighbour), the row's lse (log2 units) and D, and the L share and flux of
 // column c0 from its left interval (Lc, Fc; updated to those of c0+16).
-// Column c is a key of this row iff c <= c_last; the interval (c, c+1)
-// exists iff c + 1 <= c_last and c + 1 <= 127.
+// MASKED (tiles that cross the diagonal or the end of the sequence): column
+// c is a key of this row iff c <= c_last, and the interval (c, c+1) exists
+// iff c + 1 <= c_last.  Always: the interval (127, 128) does not exist
+// (last_chunk), and dS of columns owned by the neighbouring key tiles is 0
+// for dQ (column 0 when zero_c0, column 127).
+template <bool MASKED>
 __device__ __forceinline__ void cols16(const float (&sv)[17], const float (&gv)[17], float k2,
                                        float lse2, float Dr, float scale, int c0, int c_last,
-                                       bool zero_c0, float &Lc, float &Fc, uint32_t (&pP)[8],
-                                       uint32_t (&pS)[8]) {
+                                       bool zero_c0, bool last_chunk, float &Lc, float &Fc,
+                                       uint32_t (&pP)[8], uint32_t (&pS)[8]) {
     float u[17], pe[17];
 #pragma unroll
     for (int i = 0; i < 17; ++i) {
@@ -192,15 +193,26 @@ __device__ __forceinline__ void cols16(const float (&sv)[17], const float (&gv)[
         const int c = c0 + i;
         float R, Ln, kf;
         interval(u[i], u[i + 1], pe[i], pe[i + 1], R, Ln, kf);
-        const bool seg = c + 1 <= c_last && c + 1 <= 127;
-        R = seg ? R : 0.0f;
-        Ln = seg ? Ln : 0.0f;
-        const float Fn = seg ? kf * (gv[i] - gv[i + 1]) : 0.0f;
-        const bool key = c <= c_last;
-        const float P = key ? Lc + R : 0.0f;
-        float ds = key ? scale * fmaf(P, gv[i] - Dr, Fc - Fn) : 0.0f;
-        // columns that belong to the neighbouring key tiles take no part in dQ
-        if (c == 127 || (c == 0 && zero_c0)) ds = 0.0f;
+        float Fn = kf * (gv[i] - gv[i + 1]);
+        bool seg = true, key = true;
+        if (MASKED) {
+            seg = c + 1 <= c_last;
+            key = c <= c_last;
+        }
+        if (i == 15) seg = seg && !last_chunk;
+        if (MASKED || i == 15) {
+            R = seg ? R : 0.0f;
+            Ln = seg ? Ln : 0.0f;
+            Fn = seg ? Fn : 0.0f;
+        }
+        float P = Lc + R;
+        float ds = scale * fmaf(P, gv[i] - Dr, Fc - Fn);
+        if (MASKED) {
+            P = key ? P : 0.0f;
+            ds = key ? ds : 0.0f;
+        }
+        if (i == 0 && zero_c0) ds = 0.0f;
+        if (i == 15 && last_chunk) ds = 0.0f;
         Pv[i] = P;
         Sv[i] = ds;
         Lc = Ln;
@@ -336,8 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = j % NS;
                 const uint32_t qb = sQ + s * C::kTileBytes, gb = sG + s * C::kTileBytes;
                 if (!(ok = wait_b(BAR(C::kBarQFull + s), (j / NS) & 1, abort_flag))) break;
-                // S overwrites the dQ_part columns of the previous tile
-                if (j > 0 && !(ok = wait_b(BAR(C::kBarDqRead), (j - 1) & 1, abort_flag))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -345,6 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_mma_ss(tmem + C::kColS, make_sdesc(qb + off, 16, 1024),
                               make_sdesc(sK + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
                 }
+                // dP overwrites the dQ_part columns of the previous tile
+                if (j > 0 && !(ok = wait_b(BAR(C::kBarDqRead), (j - 1) & 1, abort_flag))) break;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
@@ -370,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    tc_mma_ss(tmem + C::kColS, make_sdesc(sS + off, 16, 1024),
+                    tc_mma_ss(tmem + C::kColP, make_sdesc(sS + off, 16, 1024),
                               make_sdesc(sK + kk * 2048, kChunkBytes, 1024), kIdQ, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(BAR(C::kBarDqFull));
@@ -389,13 +402,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_off + C::kColS, tD = tmem + lane_off + C::kColP;
         const float k2 = p.k2, scale = p.scale;
         bool ok = true;
+        // the row statistics of the first query tile; later ones are fetched
+        // one tile ahead
+        int r_next = 128 * q_first + irow;
+        float lse_next = r_next < T ? p.lse[(size_t)bh * T + r_next] : 0.0f;
+        float D_next = r_next < T ? p.Drow[(size_t)bh * T + r_next] : 0.0f;
         for (int j = 0; ok && j < nQ; ++j) {
-            const int r = 128 * (q_first + j) + irow;  // query row
+            const int row0 = 128 * (q_first + j);
+            const int r = row0 + irow;  // query row
             const bool rvalid = r < T;
-            const float lse2 = rvalid ? p.lse[(size_t)bh * T + r] * kLog2e : 0.0f;
-            const float Dr = rvalid ? p.Drow[(size_t)bh * T + r] : 0.0f;
+            const float lse2 = rvalid ? lse_next * kLog2e : 0.0f;
+            const float Dr = rvalid ? D_next : 0.0f;
+            r_next = r + 128;
+            if (j + 1 < nQ && r_next < T) {
+                lse_next = p.lse[(size_t)bh * T + r_next];
+                D_next = p.Drow[(size_t)bh * T + r_next];
+            }
             // last column of the tile this row sees (its own key, position r + 1)
             const int c_last = rvalid ? min(r + 1 - kKeyStride * kt, 127) : -1;
+            // the tile needs masks if some row of it stops before column 127
+            const bool masked = row0 + 1 - kKeyStride * kt < 127 || row0 + 127 >= T;
             ok = __all_sync(0xffffffffu, wait_b(BAR(C::kBarSFull), j & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
@@ -419,18 +445,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Lc = seg ? L : 0.0f;
                 Fc = seg ? kf * (__uint_as_float(e[2]) - __uint_as_float(e[3])) : 0.0f;
             }
-#pragma unroll
+            // four chunks of 16 columns; the TMEM loads of chunk kk+1 are in
+            // flight while chunk kk is computed
+            uint32_t a[16], g[16], an[1] = {0u}, gn[1] = {0u};
+            const int cb = 64 * half;
+            tmem_ld16(tS + cb, a);
+            tmem_ld16(tD + cb, g);
+            tmem_ld1(tS + cb + 16, an[0]);
+            tmem_ld1(tD + cb + 16, gn[0]);
+#pragma unroll 1
             for (int kk = 0; kk < 4; ++kk) {
-                const int c0 = 64 * half + 16 * kk;
-                uint32_t a[16], g[16], an[1] = {0u}, gn[1] = {0u};
-                tmem_ld16(tS + c0, a);
-                tmem_ld16(tD + c0, g);
-                if (c0 + 16 <= 127) {
-                    tmem_ld1(tS + c0 + 16, an[0]);
-                    tmem_ld1(tD + c0 + 16, gn[0]);
-                }
+                const int c0 = cb + 16 * kk;
                 wait_ld17(a, an[0]);
-                wait_ld17(g, gn[0]);  // already complete: only ties g, gn to the wait
+                wait_ld17(g, gn[0]);
                 float sv[17], gv[17];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -439,9 +466,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 sv[16] = __uint_as_float(an[0]);
                 gv[16] = __uint_as_float(gn[0]);
+                if (kk < 3) {
+                    tmem_ld16(tS + c0 + 16, a);
+                    tmem_ld16(tD + c0 + 16, g);
+                    if (c0 + 32 <= 127) {
+                        tmem_ld1(tS + c0 + 32, an[0]);
+                        tmem_ld1(tD + c0 + 32, gn[0]);
+                    }
+                }
+                const bool zero_c0 = c0 == 0 && kt > 0, last_chunk = c0 == 112;
                 uint32_t pP[8], pS[8];
-                cols16(sv, gv, k2, lse2, Dr, scale, c0, c_last, kt > 0, Lc, Fc, pP, pS);
-                // this row's 16 keys = 16-byte chunks 2*(c0%64)/16 .. +1 of box c0/64
+                if (masked)
+                    cols16<true>(sv, gv, k2, lse2, Dr, scale, c0, c_last, zero_c0, last_chunk, Lc,
+                                 Fc, pP, pS);
+                else
+                    cols16<false>(sv, gv, k2, lse2, Dr, scale, c0, c_last, zero_c0, last_chunk,
+                                  Lc, Fc, pP, pS);
+                // this row's 16 keys = 16-byte chunks ch, ch+1 of box c0/64
                 const int box = c0 >> 6, ch = (c0 & 63) >> 3;
                 uint8_t *prow = smem + C::kOffP + box * kChunkBytes + irow * 128;
                 uint8_t *srow = smem + C::kOffS + box * kChunkBytes + irow * 128;
@@ -457,7 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(BAR(C::kBarPReady));
-            // dQ_part of this query tile, added into the fp32 accumulator
+            // dQ_part of this query tile (in the dP columns), added into the
+            // fp32 accumulator
             ok = __all_sync(0xffffffffu, wait_b(BAR(C::kBarDqFull), j & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
@@ -465,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(tS + half * (D / 2) + 32 * cc, o);
+                tmem_ld32(tD + half * (D / 2) + 32 * cc, o);
                 tmem_wait_ld_regs<32>(o);
                 if (rvalid) {
 #pragma unroll

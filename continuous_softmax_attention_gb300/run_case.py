@@ -6,7 +6,8 @@
 Inputs come from the seeded generator; each iteration launches the
 continuous kernel once and, unless --no-std, the standard kernel once.
 With --decode each iteration is one decode step (lengths drawn from
-[T/2, T]).
+[T/2, T]); with --backward one forward pass, then each iteration is one
+backward pass.
 """
 from __future__ import annotations
 
@@ -29,9 +30,12 @@ def main():
     ap.add_argument("--iters", type=int, default=2)
     ap.add_argument("--no-std", action="store_true")
     ap.add_argument("--decode", action="store_true")
+    ap.add_argument("--backward", action="store_true")
     a = ap.parse_args()
     if a.decode:
         return run_decode(a)
+    if a.backward:
+        return run_backward(a)
     x = make_inputs(a.B, a.H, a.T, a.d, "bf16", seed=0)
     g = {k: v.cuda() for k, v in x.items()}
     scale = 1.0 / math.sqrt(a.d)
@@ -42,6 +46,23 @@ def main():
     torch.cuda.synchronize()
     st = csa.device_status()
     print(f"ok status={st} o_mean={o.float().abs().mean().item():.5f}")
+    if st != 0:
+        raise SystemExit(1)
+
+
+def run_backward(a):
+    x = make_inputs(a.B, a.H, a.T, a.d, "bf16", seed=0)
+    g = {k: v.cuda() for k, v in x.items()}
+    scale = 1.0 / math.sqrt(a.d)
+    o, lse = csa.forward(g["q"], g["k"], g["v"], g["k0"], g["v0"], mode=a.mode, scale=scale)
+    dout = torch.randn(a.B, a.H, a.T, a.d, generator=torch.Generator().manual_seed(1))
+    dout = dout.to(torch.bfloat16).cuda()
+    for _ in range(a.iters):
+        dq, dk, dv, _, _ = csa.backward(g["q"], g["k"], g["v"], o, lse, dout, g["k0"], g["v0"],
+                                        mode=a.mode, scale=scale)
+    torch.cuda.synchronize()
+    st = csa.device_status()
+    print(f"ok status={st} dq_mean={dq.float().abs().mean().item():.5f}")
     if st != 0:
         raise SystemExit(1)
 
