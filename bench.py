@@ -64,6 +64,8 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "csa_forward_headline.md")
 KERNEL_SOURCES = ["csa_tc.cu", "csa_tc_common.cuh", "csa_device.cuh"]
 DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_chunk_bench.md")
 DECODE_SOURCES = ["csa_decode.cu", "csa_device.cuh"]
+BACKWARD_PROFILE = os.path.join(ROOT, "profiles", "backward_headline.md")
+BACKWARD_SOURCES = ["csa_tc_bwd.cu", "csa_tc_common.cuh", "csa_device.cuh"]
 
 
 def kernel_source_hash(names=KERNEL_SOURCES):
@@ -356,6 +358,8 @@ class BackwardBench:
         tot = max_over_ranks(sum(self.ms), device=dev)
         ms = tot / steps
         achieved = flops / (ms * 1e-3) / 1e12
+        per_head = recorded_figure(BACKWARD_PROFILE, "traffic_bytes_per_head", BACKWARD_SOURCES)
+        traffic = None if per_head is None else int(per_head * B * H)
         return {
             "metric": f"continuous-attn bwd TFLOP/s (B={B},H={H},T={T},d={d}, bf16, causal)",
             "value": round(world * achieved, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
@@ -363,7 +367,10 @@ class BackwardBench:
             "flops_per_step": flops,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                         "peak_source": f"{src} bf16 dense (burst)", "traffic": None,
+                         "peak_source": f"{src} bf16 dense (burst)", "traffic": traffic,
+                         "traffic_unit": "bytes per call (ncu dram read+write of the tensor-core "
+                                         "kernel per head, times this workload's heads)",
+                         "algorithmic_bytes": 2 * 8 * B * H * T * d + 4 * B * H * T,
                          "timed": "whole csa_backward call (D row dot, tensor-core kernel, dq "
                                   "conversion)"},
             "gpu_launches_per_step": self.launches,
