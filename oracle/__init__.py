@@ -13,6 +13,8 @@ What it computes follows Jianlin Su, "Continuous Softmax Attention"
 * ``forward_eq11``   - eq. (10)/(11), the softmax of ``a + b``.
 * ``forward_rows``   - eq. (8) for selected rows only (large shapes).
 * ``std_forward``    - eq. (12), standard causal softmax attention.
+* ``forward_short_conv`` - the short-conv reading of eq. (13): b replaced by
+                       its first-order Taylor term (a cheaper variant).
 * ``row_bias``       - the logits ``a`` and corrections ``b`` of eq. (10)
                        for one row.
 * ``phi1``/``phi2``/``log_phi1``/``log_phi2`` - eq. (6) and its limits.
@@ -70,6 +72,10 @@ def _load():
     lib.csa_oracle_std_forward_rows.restype = i
     lib.csa_oracle_row_bias.argtypes = [p, p, p, i, i, i, i, d, i, i, i, i, p, p]
     lib.csa_oracle_row_bias.restype = i
+    lib.csa_oracle_forward_short_conv.argtypes = common
+    lib.csa_oracle_forward_short_conv.restype = i
+    lib.csa_oracle_forward_short_conv_rows.argtypes = [p, p, p, p, p, p, ll, p, p, i, i, i, i, d, i, i]
+    lib.csa_oracle_forward_short_conv_rows.restype = i
     lib.csa_oracle_log_dphi2.restype = d
     lib.csa_oracle_log_dphi2.argtypes = [d]
     lib.csa_oracle_backward.argtypes = [p, p, p, p, p, p, p, p, p, p, p, i, i, i, i, d, i, i]
@@ -156,6 +162,33 @@ def forward_eq11(q, k, v, k0=None, v0=None, scale=None, mode=ZERO, nthreads=None
     if scale is None:
         scale = 1.0 / np.sqrt(_f32(q).shape[-1])
     return _run(_load().csa_oracle_forward_eq11, q, k, v, k0, v0, scale, mode, nthreads)
+
+
+def forward_short_conv(q, k, v, k0=None, v0=None, scale=None, mode=ZERO, nthreads=None):
+    """The short-conv reading of eq. (13): b replaced by its first-order
+    Taylor term ((a_{i-1} + a_{i+1} - 2 a_i)/6 inside, -log 2 + step/3 at the
+    two ends).  Returns (o, lse)."""
+    if scale is None:
+        scale = 1.0 / np.sqrt(_f32(q).shape[-1])
+    return _run(_load().csa_oracle_forward_short_conv, q, k, v, k0, v0, scale, mode, nthreads)
+
+
+def forward_short_conv_rows(q, k, v, rows, k0=None, v0=None, scale=None, mode=ZERO,
+                            nthreads=None):
+    """forward_short_conv for the flat rows given.  Returns (o[nrows, d], lse[nrows])."""
+    q, k, v, k0, v0, (B, H, T, d) = _prep(q, k, v, k0, v0, mode)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = rows.shape[0]
+    out = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    rc = _load().csa_oracle_forward_short_conv_rows(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(k0), _ptr(v0), _ptr(rows), n, _ptr(out), _ptr(lse), B, H,
+        T, d, float(scale), int(mode), int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return out, lse
 
 
 def std_forward(q, k, v, scale=None, nthreads=None):

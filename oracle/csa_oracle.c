@@ -102,7 +102,7 @@ typedef struct {
     /* explicit row list (NULL = all rows) */
     const long long *rows;
     long long nrows;
-    int form; /* 0 = eq.(8), 1 = eq.(11), 2 = eq.(12) standard */
+    int form; /* 0 = eq.(8), 1 = eq.(11), 2 = eq.(12) standard, 3 = eq.(13) short conv */
 } job_t;
 
 typedef struct {
@@ -195,6 +195,38 @@ static void one_row(const job_t *jb, long long flat, double *out_row, double *ls
         }
         for (int c = 0; c < d; ++c) out_row[c] = num[c] / den;
         if (lse_out) *lse_out = m + log(den);
+        return;
+    }
+
+    if (jb->form == 3) {
+        /* The short-conv reading of eq.(13): b replaced by its first-order
+         * Taylor term.  Interior keys: log(phi2(x) + phi2(y)) with
+         * phi2(x) = 1/2 + x/6 + O(x^2) gives b_i = (a_{i-1} + a_{i+1} - 2 a_i)/6;
+         * the end keys (one phi2 each): log phi2(x) = -log 2 + x/3 + O(x^2)
+         * gives b_0 = -log 2 + (a_1 - a_0)/3, b_t = -log 2 + (a_{t-1} - a_t)/3.
+         * Then a plain two-pass softmax over z = a + b. */
+        double zmax = -INFINITY;
+        double *z = a + (t + 1);
+        for (int i = 0; i <= t; ++i) {
+            double b;
+            if (i == 0)
+                b = -log(2.0) + (a[1] - a[0]) / 3.0;
+            else if (i == t)
+                b = -log(2.0) + (a[t - 1] - a[t]) / 3.0;
+            else
+                b = (a[i - 1] + a[i + 1] - 2.0 * a[i]) / 6.0;
+            z[i] = a[i] + b;
+            if (z[i] > zmax) zmax = z[i];
+        }
+        double den = 0.0;
+        for (int i = 0; i <= t; ++i) {
+            const double w = exp(z[i] - zmax);
+            const float *vi = val_ptr(jb, bh, i, h, zero);
+            for (int c = 0; c < d; ++c) num[c] += w * (double)vi[c];
+            den += w;
+        }
+        for (int c = 0; c < d; ++c) out_row[c] = num[c] / den;
+        if (lse_out) *lse_out = zmax + log(den);
         return;
     }
 
@@ -353,6 +385,24 @@ int csa_oracle_forward_eq11(const float *q, const float *k, const float *v, cons
                             double scale, int k0_mode, int nthreads)
 {
     return forward_common(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, NULL, 0, 1, nthreads);
+}
+
+/* The short-conv reading of eq.(13): b replaced by its first-order term. */
+int csa_oracle_forward_short_conv(const float *q, const float *k, const float *v, const float *k0,
+                                  const float *v0, double *out, double *lse, int B, int H, int T,
+                                  int d, double scale, int k0_mode, int nthreads)
+{
+    return forward_common(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, NULL, 0, 3, nthreads);
+}
+
+/* eq.(13) short conv for a list of rows only. */
+int csa_oracle_forward_short_conv_rows(const float *q, const float *k, const float *v,
+                                       const float *k0, const float *v0, const long long *rows,
+                                       long long nrows, double *out, double *lse, int B, int H,
+                                       int T, int d, double scale, int k0_mode, int nthreads)
+{
+    if (!rows && nrows > 0) return -1;
+    return forward_common(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, rows, nrows, 3, nthreads);
 }
 
 /* Standard causal softmax attention, eq.(12). */
