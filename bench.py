@@ -216,6 +216,8 @@ def run_gpu(args):
         return ms
 
     csa_call = lambda: csa.forward(g["q"], g["k"], g["v"], mode=w.modes[0], scale=scale, out=out, lse=lse)
+    sc_call = lambda: csa.forward(g["q"], g["k"], g["v"], mode=w.modes[0], scale=scale, out=out,
+                                  lse=lse, short_conv=True)
     std_call = lambda: csa.std_forward(g["q"], g["k"], g["v"], scale=scale, out=out, lse=lse)
 
     dec = None if args.no_decode else DecodeBench(csa, dev, stream, flush)
@@ -241,6 +243,7 @@ def run_gpu(args):
     for _ in range(args.warmup):
         csa_call()
         std_call()
+        sc_call()
         e2e_call()
         if dec is not None:
             dec.call()
@@ -255,6 +258,7 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         ms_csa = timed(csa_call, args.steps)
         ms_std = timed(std_call, args.steps)
+        ms_sc = timed(sc_call, args.steps)
         ms_e2e = timed(e2e_call, args.steps)
         if dec is not None:
             dec.ms = timed(dec.call, args.decode_steps)
@@ -269,6 +273,7 @@ def run_gpu(args):
         return max_over_ranks(sum(ms), device=dev)
 
     tot_csa, tot_std, tot_e2e = total(ms_csa), total(ms_std), total(ms_e2e)
+    tot_sc = total(ms_sc)
     if ws > 1:
         dist.destroy_process_group()
     if rank != 0:
@@ -303,7 +308,11 @@ def run_gpu(args):
                 "ratio_continuous_over_std": round(value / std_value, 4)},
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "ms_per_step": round(tot_e2e / K, 5),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 3 * K + (0 if dec is None else 2 * 2 * args.decode_steps) +
+        "short_conv": {"value": round(ws * flops * K / (tot_sc * 1e-3) / 1e12, 3), "unit": UNIT,
+                       "ms_per_step": round(tot_sc / K, 5),
+                       "ratio_over_std": round((flops / tot_sc) / (flops_std / tot_std), 4),
+                       "note": "first-order (eq. (13)) reading of the same step, csa_forward_short_conv"},
+        "gpu_launches": 4 * K + (0 if dec is None else 2 * 2 * args.decode_steps) +
                         (0 if bwd is None else bwd.launches * args.backward_steps),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": burst,
                      "unit": "TFLOP/s", "frac": round(achieved / burst, 4),

@@ -49,6 +49,7 @@ def load():
     std = [p, p, p, p, p, i, i, i, i, f, p]
     bwd = [p, p, p, p, p, p, p, p, p, p, p, p, p, p, ctypes.c_longlong, i, i, i, i, f, i, p]
     for name, args in (("csa_forward", fwd), ("csa_forward_f32", fwd),
+                       ("csa_forward_short_conv", fwd), ("csa_forward_short_conv_f32", fwd),
                        ("csa_std_forward", std), ("csa_std_forward_f32", std),
                        ("csa_logphi2_eval", [p, p, i, p]),
                        ("csa_segment_weights_eval", [p, p, p, p, i, p]),
@@ -114,13 +115,14 @@ def _check_tensor(t, name, dtype, shape, device):
 
 
 def forward(q, k, v, k0=None, v0=None, *, mode: int = 0, scale=None, out=None, lse=None,
-            stream=None, want_lse: bool = True):
+            stream=None, want_lse: bool = True, short_conv: bool = False):
     """Causal continuous softmax attention.  Returns (o, lse).
 
     q, k, v: CUDA tensors [B, H, T, d], all bf16 (tensor-core kernel for
     d in {64, 128}) or all fp32 (CUDA-core kernel).  k0, v0: [H, d], read
     in mode GIVEN (2).  mode: 0 zero sink, 1 copy of the first token,
-    2 given.  scale defaults to 1/sqrt(d)."""
+    2 given.  scale defaults to 1/sqrt(d).  short_conv=True runs the
+    first-order (eq. (13)) reading instead (csa_forward_short_conv)."""
     import torch
 
     B, H, T, d = q.shape
@@ -145,12 +147,11 @@ def forward(q, k, v, k0=None, v0=None, *, mode: int = 0, scale=None, out=None, l
     if lse is not None:
         _check_tensor(lse, "lse", torch.float32, (B, H, T), dev)
     lib = load()
-    if dtype == torch.bfloat16:
-        fn, where = lib.csa_forward, "csa_forward"
-    elif dtype == torch.float32:
-        fn, where = lib.csa_forward_f32, "csa_forward_f32"
-    else:
+    if dtype not in (torch.bfloat16, torch.float32):
         raise ValueError(f"unsupported dtype {dtype}")
+    where = ("csa_forward_short_conv" if short_conv else "csa_forward") + (
+        "" if dtype == torch.bfloat16 else "_f32")
+    fn = getattr(lib, where)
     _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(k0), _ptr(v0), _ptr(out), _ptr(lse),
               B, H, T, d, float(scale), int(mode), _stream_handle(stream)), where)
     return out, lse

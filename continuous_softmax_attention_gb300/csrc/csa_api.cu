@@ -49,7 +49,8 @@ int from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; 
 
 int forward_bf16(const void *q, const void *k, const void *v, const void *k0, const void *v0,
                  void *out, float *lse, int B, int H, int T, int d, float scale, int mode,
-                 bool continuous, csa_stream_t stream) {
+                 int form, csa_stream_t stream) {
+    const bool continuous = form != kFormStd;
     bool empty;
     int rc = check_common(q, k, v, k0, v0, out, B, H, T, d, scale, mode, continuous, &empty);
     if (rc != CSA_OK || empty) return rc;
@@ -63,16 +64,18 @@ int forward_bf16(const void *q, const void *k, const void *v, const void *k0, co
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (d == 64 || d == 128) {
         if (scale < 0.0f) return CSA_ERR_UNSUPPORTED;
-        if (continuous) return csa_tc_forward(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, s);
+        if (continuous)
+            return csa_tc_forward(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, form, s);
         return csa_tc_std_forward(q, k, v, out, lse, B, H, T, d, scale, s);
     }
     return from_cuda(csa_simt_forward_bf16(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode,
-                                           continuous, s));
+                                           form, s));
 }
 
 int forward_f32(const float *q, const float *k, const float *v, const float *k0, const float *v0,
                 float *out, float *lse, int B, int H, int T, int d, float scale, int mode,
-                bool continuous, csa_stream_t stream) {
+                int form, csa_stream_t stream) {
+    const bool continuous = form != kFormStd;
     bool empty;
     int rc = check_common(q, k, v, k0, v0, out, B, H, T, d, scale, mode, continuous, &empty);
     if (rc != CSA_OK || empty) return rc;
@@ -82,7 +85,7 @@ int forward_f32(const float *q, const float *k, const float *v, const float *k0,
         return CSA_ERR_ALIGNMENT;
     if ((rc = device_ok()) != CSA_OK) return rc;
     return from_cuda(csa_simt_forward_f32(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode,
-                                          continuous, reinterpret_cast<cudaStream_t>(stream)));
+                                          form, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int decode_bf16(const void *q, const void *k_cache, const void *v_cache, const void *k0,
@@ -211,25 +214,39 @@ int csa_decode(const void *q, const void *k_cache, const void *v_cache, const vo
 int csa_forward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
                 void *out, float *lse, int B, int H, int T, int d, float scale, int k0_mode,
                 csa_stream_t stream) {
-    return forward_bf16(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, true, stream);
+    return forward_bf16(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, kFormExact, stream);
+}
+
+int csa_forward_short_conv(const void *q, const void *k, const void *v, const void *k0,
+                           const void *v0, void *out, float *lse, int B, int H, int T, int d,
+                           float scale, int k0_mode, csa_stream_t stream) {
+    return forward_bf16(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, kFormShortConv,
+                        stream);
+}
+
+int csa_forward_short_conv_f32(const float *q, const float *k, const float *v, const float *k0,
+                               const float *v0, float *out, float *lse, int B, int H, int T,
+                               int d, float scale, int k0_mode, csa_stream_t stream) {
+    return forward_f32(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, kFormShortConv,
+                       stream);
 }
 
 int csa_forward_f32(const float *q, const float *k, const float *v, const float *k0,
                     const float *v0, float *out, float *lse, int B, int H, int T, int d,
                     float scale, int k0_mode, csa_stream_t stream) {
-    return forward_f32(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, true, stream);
+    return forward_f32(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, kFormExact, stream);
 }
 
 int csa_std_forward(const void *q, const void *k, const void *v, void *out, float *lse, int B,
                     int H, int T, int d, float scale, csa_stream_t stream) {
-    return forward_bf16(q, k, v, nullptr, nullptr, out, lse, B, H, T, d, scale, CSA_K0_ZERO, false,
-                        stream);
+    return forward_bf16(q, k, v, nullptr, nullptr, out, lse, B, H, T, d, scale, CSA_K0_ZERO,
+                        kFormStd, stream);
 }
 
 int csa_std_forward_f32(const float *q, const float *k, const float *v, float *out, float *lse,
                         int B, int H, int T, int d, float scale, csa_stream_t stream) {
-    return forward_f32(q, k, v, nullptr, nullptr, out, lse, B, H, T, d, scale, CSA_K0_ZERO, false,
-                       stream);
+    return forward_f32(q, k, v, nullptr, nullptr, out, lse, B, H, T, d, scale, CSA_K0_ZERO,
+                       kFormStd, stream);
 }
 
 int csa_logphi2_eval(const float *x, float *y, int n, csa_stream_t stream) {

@@ -4,22 +4,25 @@
 
 #include <cuda_runtime.h>
 
-// CUDA-core kernels (csa_simt.cu).  continuous = false gives eq. (12).
+// Forms of the forward pass: eq. (10)/(11), the short-conv reading of
+// eq. (13) (b replaced by its first-order term), eq. (12).
+enum { kFormExact = 0, kFormShortConv = 1, kFormStd = 2 };
+
+// CUDA-core kernels (csa_simt.cu).
 cudaError_t csa_simt_forward_f32(const float *q, const float *k, const float *v, const float *k0,
                                  const float *v0, float *out, float *lse, int B, int H, int T,
-                                 int d, float scale, int mode, bool continuous,
-                                 cudaStream_t stream);
+                                 int d, float scale, int mode, int form, cudaStream_t stream);
 cudaError_t csa_simt_forward_bf16(const void *q, const void *k, const void *v, const void *k0,
                                   const void *v0, void *out, float *lse, int B, int H, int T,
-                                  int d, float scale, int mode, bool continuous,
-                                  cudaStream_t stream);
+                                  int d, float scale, int mode, int form, cudaStream_t stream);
 cudaError_t csa_simt_logphi2_eval(const float *x, float *y, int n, cudaStream_t stream);
 
 // Tensor-core kernels, d in {64, 128}, bf16.  Return a CSA_* status code
-// (CSA_OK on success).  Continuous attention (csa_tc.cu):
+// (CSA_OK on success).  Continuous attention, form kFormExact or
+// kFormShortConv (csa_tc.cu):
 int csa_tc_forward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
                    void *out, float *lse, int B, int H, int T, int d, float scale, int mode,
-                   cudaStream_t stream);
+                   int form, cudaStream_t stream);
 // Standard causal attention, eq. (12) (csa_tc_std.cu):
 int csa_tc_std_forward(const void *q, const void *k, const void *v, void *out, float *lse, int B,
                        int H, int T, int d, float scale, cudaStream_t stream);

@@ -1,5 +1,6 @@
 // CUDA-core kernels: continuous attention (eq. (10)/(11) of Jianlin Su,
-// "Continuous Softmax Attention") and standard causal attention (eq. (12)),
+// "Continuous Softmax Attention"), its short-conv reading (b replaced by the
+// first-order term of eq. (13)) and standard causal attention (eq. (12)),
 // for fp32 inputs and for bf16 inputs whose head dimension the tensor-core
 // kernel does not cover.
 //
@@ -133,7 +134,8 @@ struct RowIO {
 };
 
 // grid: one warp per (b, h, row); rows handed out longest first.
-template <typename Tin, int NPL, bool CONT>
+// FORM: 0 eq. (10)/(11), 1 the short-conv reading of eq. (13), 2 eq. (12).
+template <typename Tin, int NPL, int FORM>
 __global__ void __launch_bounds__(256) simt_forward_kernel(const Tin *q, const Tin *k,
                                                            const Tin *v, const Tin *k0,
                                                            const Tin *v0, Tin *out, float *lse,
@@ -158,14 +160,23 @@ __global__ void __launch_bounds__(256) simt_forward_kernel(const Tin *q, const T
     RowAcc<NPL> acc;
     float vv[NPL];
     const int t = r + 1;  // the page's token index
-    if (CONT) {
-        // keys i = 0..t with b from eq. (10)
+    if (FORM != 2) {
+        // keys i = 0..t with b from eq. (10), or its first-order term
         float a_prev = 0.0f;
         float a_cur = io.logit(io.key(0), scale);
         float a_next = io.logit(io.key(1), scale);
         for (int i = 0; i <= t; ++i) {
             float b;
-            if (i == 0) {
+            if (FORM == 1) {
+                // log phi2(x) = -log 2 + x/3 + ..; log(phi2(x) + phi2(y)) = (x + y)/6 + ..
+                constexpr float kLn2f = 0.69314718055994531f;
+                if (i == 0)
+                    b = (a_next - a_cur) * (1.0f / 3.0f) - kLn2f;
+                else if (i == t)
+                    b = (a_prev - a_cur) * (1.0f / 3.0f) - kLn2f;
+                else
+                    b = (a_prev + a_next - 2.0f * a_cur) * (1.0f / 6.0f);
+            } else if (i == 0) {
                 b = log_phi2_f32(a_next - a_cur);
             } else if (i == t) {
                 b = log_phi2_f32(a_prev - a_cur);
@@ -201,51 +212,55 @@ __global__ void logphi2_eval_kernel(const float *x, float *y, int n) {
     if (i < n) y[i] = log_phi2_f32(x[i]);
 }
 
-template <typename Tin, bool CONT, int NPL>
+template <typename Tin, int FORM, int NPL>
 cudaError_t launch_npl(const Tin *q, const Tin *k, const Tin *v, const Tin *k0, const Tin *v0,
                        Tin *out, float *lse, int B, int H, int T, int d, float scale, int mode,
                        cudaStream_t stream) {
     const long long rows = (long long)B * H * T;
     const int threads = 256;
     const long long blocks = (rows + 7) / 8;
-    simt_forward_kernel<Tin, NPL, CONT><<<(unsigned)blocks, threads, 0, stream>>>(
+    simt_forward_kernel<Tin, NPL, FORM><<<(unsigned)blocks, threads, 0, stream>>>(
         q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode);
     return cudaGetLastError();
 }
 
-template <typename Tin, bool CONT>
+template <typename Tin, int FORM>
 cudaError_t launch_any(const Tin *q, const Tin *k, const Tin *v, const Tin *k0, const Tin *v0,
                        Tin *out, float *lse, int B, int H, int T, int d, float scale, int mode,
                        cudaStream_t stream) {
-    if (d <= 32) return launch_npl<Tin, CONT, 1>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
-    if (d <= 64) return launch_npl<Tin, CONT, 2>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
-    if (d <= 128) return launch_npl<Tin, CONT, 4>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
-    return launch_npl<Tin, CONT, 8>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
+    if (d <= 32) return launch_npl<Tin, FORM, 1>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
+    if (d <= 64) return launch_npl<Tin, FORM, 2>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
+    if (d <= 128) return launch_npl<Tin, FORM, 4>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
+    return launch_npl<Tin, FORM, 8>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
 }
 
 }  // namespace
 
 cudaError_t csa_simt_forward_f32(const float *q, const float *k, const float *v, const float *k0,
                                  const float *v0, float *out, float *lse, int B, int H, int T,
-                                 int d, float scale, int mode, bool continuous,
+                                 int d, float scale, int mode, int form,
                                  cudaStream_t stream) {
-    if (continuous)
-        return launch_any<float, true>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
-    return launch_any<float, false>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
+    if (form == 0)
+        return launch_any<float, 0>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
+    if (form == 1)
+        return launch_any<float, 1>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
+    return launch_any<float, 2>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
 }
 
 cudaError_t csa_simt_forward_bf16(const void *q, const void *k, const void *v, const void *k0,
                                   const void *v0, void *out, float *lse, int B, int H, int T,
-                                  int d, float scale, int mode, bool continuous,
+                                  int d, float scale, int mode, int form,
                                   cudaStream_t stream) {
     using bf = __nv_bfloat16;
     const bf *q_ = static_cast<const bf *>(q), *k_ = static_cast<const bf *>(k);
     const bf *v_ = static_cast<const bf *>(v), *k0_ = static_cast<const bf *>(k0);
     const bf *v0_ = static_cast<const bf *>(v0);
     bf *o_ = static_cast<bf *>(out);
-    if (continuous)
-        return launch_any<bf, true>(q_, k_, v_, k0_, v0_, o_, lse, B, H, T, d, scale, mode, stream);
-    return launch_any<bf, false>(q_, k_, v_, k0_, v0_, o_, lse, B, H, T, d, scale, mode, stream);
+    if (form == 0)
+        return launch_any<bf, 0>(q_, k_, v_, k0_, v0_, o_, lse, B, H, T, d, scale, mode, stream);
+    if (form == 1)
+        return launch_any<bf, 1>(q_, k_, v_, k0_, v0_, o_, lse, B, H, T, d, scale, mode, stream);
+    return launch_any<bf, 2>(q_, k_, v_, k0_, v0_, o_, lse, B, H, T, d, scale, mode, stream);
 }
 
 cudaError_t csa_simt_logphi2_eval(const float *x, float *y, int n, cudaStream_t stream) {

@@ -38,6 +38,11 @@
 // All weights carry a common factor (ln 2)^2, which cancels in o and is
 // removed from lse.
 //
+// The template flag SHORT turns the kernel into the short-conv reading of
+// eq. (13): b is replaced by its first-order term, so a key's weight is
+// 2^z with z an affine combination of its own and its neighbours' logits
+// (short_chunk) and no phi2 is formed.
+//
 // The two column halves of a row exchange their partial maxima, the L share
 // that crosses into the next tile, and their final sums through shared
 // memory, synchronised by an mbarrier.  Every mbarrier wait is bounded in
@@ -190,6 +195,46 @@ __device__ __forceinline__ void cont_chunk(const float (&sv)[33], float k2, floa
     Lc = L[32];
 }
 
+// The short-conv reading of eq. (13): a key's weight is 2^z, with z in log2
+// units relative to the running max and b replaced by its first-order term:
+//   inside the row   z = (4 u_c + u_{c-1} + u_{c+1}) / 6
+//   one-sided ends   z = (2 u_c + u_nb) / 3 - 1   (the sink; each row's last key)
+// (-1 is log2 of the 1/2 in log phi2(x) = -log 2 + x/3 + ...).  Every z is a
+// convex combination of logits minus a constant, so the running max of the
+// raw logits still bounds it.  sv[0..32] are the raw logits of columns
+// cbase..cbase+32, sl that of column cbase-1 (unused when first_end: the
+// sink).  Produces w[0..31].
+template <bool MASKED>
+__device__ __forceinline__ void short_chunk(const float (&sv)[33], float sl, float k2, float nm,
+                                            int cbase, int c_last, bool first_end,
+                                            float (&w)[32]) {
+    constexpr float kThird = 1.0f / 3.0f, kSixth = 1.0f / 6.0f;
+    float u[34];
+    u[0] = fmaf(sl, k2, nm);
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const float2 t = __ffma2_rn(make_float2(sv[i], sv[i + 1]), make_float2(k2, k2),
+                                    make_float2(nm, nm));
+        u[i + 1] = t.x;
+        u[i + 2] = t.y;
+    }
+    u[33] = fmaf(sv[32], k2, nm);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float ul = u[i], uc = u[i + 1], ur = u[i + 2];
+        float z = fmaf(ul + ur, kSixth, 4.0f * kSixth * uc);
+        if (i == 0 && first_end) z = fmaf(ur, kThird, fmaf(2.0f * kThird, uc, -1.0f));
+        if (MASKED) {
+            const int c = cbase + i;
+            const float zl = fmaf(ul, kThird, fmaf(2.0f * kThird, uc, -1.0f));
+            z = c == c_last ? zl : z;
+            w[i] = c <= c_last ? ex2_approx(z) : 0.0f;
+        } else {
+            w[i] = ex2_approx(z);
+        }
+    }
+}
+
 // Per-row online-softmax state of one softmax thread.
 struct RowState {
     float k2;      // scale * log2(e)
@@ -232,12 +277,18 @@ __device__ __forceinline__ uint32_t p_col(int k) { return k < 2 ? 16u * k : 80u 
 // of its first key).  Lc enters as the L share of the half's first key
 // coming from the left and leaves (half 1) as that of the halo key, the
 // next tile's first key.
-template <bool MASKED>
+// SHORT: the short-conv reading of eq. (13) (short_chunk); Lc then carries
+// raw logits instead of L shares: in, the logit of the column left of the
+// half's first key (for half 0 of the first tile: none, the sink is an end);
+// out (half 1), that of column 126, the left neighbour of the next tile's
+// first key.  tile0: this is the first key tile (column 0 is the sink).
+template <bool MASKED, bool SHORT>
 __device__ __forceinline__ void half_weights(uint32_t tS, const uint32_t (&a)[2][32], uint32_t nb,
                                              RowState &st, int half, int c_last, int sink,
-                                             float nm, float &Lc) {
+                                             bool tile0, float nm, float &Lc) {
     const float k2 = st.k2;
-    if (half == 1) {
+    if (SHORT && half == 1) Lc = __uint_as_float(nb);  // column 63
+    if (!SHORT && half == 1) {
         // interval (63, 64) gives key 64 its share from the left
         const float u0 = fmaf(__uint_as_float(nb), k2, nm);
         const float u1 = fmaf(__uint_as_float(a[0][0]), k2, nm);
@@ -259,9 +310,15 @@ __device__ __forceinline__ void half_weights(uint32_t tS, const uint32_t (&a)[2]
         if (k == 0 && sink == 1) sv[0] = sv[1];       // k_0 = k_1
         if (k == 0 && sink == 2) sv[0] = st.s_sink;   // given k_0
         float w[32], L31;
-        cont_chunk<MASKED>(sv, k2, nm, 32 * k, c_last, Lc, L31, w);
+        if (SHORT) {
+            short_chunk<MASKED>(sv, Lc, k2, nm, 32 * k, c_last, k == 0 && tile0, w);
+            L31 = sv[30];  // column 126 when k == 3
+            Lc = sv[31];   // left neighbour of the next chunk
+        } else {
+            cont_chunk<MASKED>(sv, k2, nm, 32 * k, c_last, Lc, L31, w);
+        }
         if (k == 3) {
-            Lc = L31;  // L share of the halo key = next tile's first key
+            Lc = L31;  // carried to the next tile's first key
             w[31] = 0.0f;
         }
         if (k == 0 && sink == 1) {  // v_0 = v_1: the sink's weight lands on key 1
@@ -289,7 +346,7 @@ __device__ __forceinline__ void half_weights(uint32_t tS, const uint32_t (&a)[2]
     st.l_run += lsum.x + lsum.y;
 }
 
-template <int D>
+template <int D, bool SHORT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_forward_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -534,13 +591,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st.m_run = mt;
                 st.l_run *= alpha;
                 st.w_sink *= alpha;
-                Lc *= alpha;
+                if (!SHORT) Lc *= alpha;  // SHORT carries a raw logit
             }
             const float nm = -st.m_run;
             if (masked)
-                half_weights<true>(tS, a, nb[0], st, half, c_last, sink, nm, Lc);
+                half_weights<true, SHORT>(tS, a, nb[0], st, half, c_last, sink, j == 0, nm, Lc);
             else
-                half_weights<false>(tS, a, nb[0], st, half, c_last, sink, nm, Lc);
+                half_weights<false, SHORT>(tS, a, nb[0], st, half, c_last, sink, j == 0, nm, Lc);
             if (half == 1) xcarry[(xe & 1) * 128 + irow] = Lc;
             // Rescale O (this half's value columns; half 1 also the row-sum
             // column) when the max moved, after PV(j-1) finished.
@@ -621,7 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (store && half == 0 && p.lse)
-                    p.lse[(size_t)bh * T + r] = (st.m_run + log2f(l_run)) * kLn2 + kLseShift;
+                    p.lse[(size_t)bh * T + r] =
+                        (st.m_run + log2f(l_run)) * kLn2 + (SHORT ? 0.0f : kLseShift);
             }
         }
     }
@@ -663,7 +721,7 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns) {
 }
 
 // ---------------------------------------------------------------- host side
-template <int D>
+template <int D, bool SHORT>
 int launch_tc(const void *q, const void *k, const void *v, const void *k0, const void *v0,
               void *out, float *lse, int B, int H, int T, float scale, int mode,
               cudaStream_t stream) {
@@ -687,7 +745,7 @@ int launch_tc(const void *q, const void *k, const void *v, const void *k0, const
     prm.lse = lse;
     const long long grid = (long long)prm.num_qtiles * BH;
     if (grid > 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
-    auto kern = tc_forward_kernel<D>;
+    auto kern = tc_forward_kernel<D, SHORT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return CSA_ERR_CUDA;
@@ -699,9 +757,12 @@ int launch_tc(const void *q, const void *k, const void *v, const void *k0, const
 
 int csa_tc_forward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
                    void *out, float *lse, int B, int H, int T, int d, float scale, int mode,
-                   cudaStream_t stream) {
-    if (d == 128) return launch_tc<128>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
-    if (d == 64) return launch_tc<64>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
+                   int form, cudaStream_t stream) {
+    const bool sc = form == kFormShortConv;
+    if (d == 128 && !sc) return launch_tc<128, false>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
+    if (d == 64 && !sc) return launch_tc<64, false>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
+    if (d == 128) return launch_tc<128, true>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
+    if (d == 64) return launch_tc<64, true>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
     return CSA_ERR_UNSUPPORTED;
 }
 

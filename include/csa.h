@@ -103,6 +103,28 @@ int csa_forward_f32(const float *q, const float *k, const float *v, const float 
                     float scale, int k0_mode, csa_stream_t stream);
 
 /*
+ * csa_forward_short_conv - the short-conv reading of eq. (13) ("Analysis of
+ *   the Result" of "Continuous Softmax Attention"): the correction b is
+ *   replaced by its first-order Taylor term, which the page likens to a
+ *   short convolution over the attention logits:
+ *       b_{t,i} = (a_{t,i-1} + a_{t,i+1} - 2 a_{t,i}) / 6      1 <= i <= t-1
+ *       b_{t,0} = -log 2 + (a_{t,1} - a_{t,0}) / 3
+ *       b_{t,t} = -log 2 + (a_{t,t-1} - a_{t,t}) / 3
+ *   (the ends from log phi2(x) = -log 2 + x/3 + O(x^2)); o and lse as in
+ *   eq. (11).  It agrees with csa_forward to second order in the logit
+ *   steps and forms no phi2, so it runs faster.  Same arguments, layout,
+ *   alignment, d rules, sink modes and errors as csa_forward.
+ */
+int csa_forward_short_conv(const void *q, const void *k, const void *v, const void *k0,
+                           const void *v0, void *out, float *lse, int B, int H, int T, int d,
+                           float scale, int k0_mode, csa_stream_t stream);
+
+/* csa_forward_short_conv_f32 - the same in fp32 on CUDA cores, 1 <= d <= 256. */
+int csa_forward_short_conv_f32(const float *q, const float *k, const float *v, const float *k0,
+                               const float *v0, float *out, float *lse, int B, int H, int T,
+                               int d, float scale, int k0_mode, csa_stream_t stream);
+
+/*
  * csa_std_forward - standard causal softmax attention (b = 0, no sink),
  *   bf16 inputs, tensor-core path.
  *   Defines: eq. (12) of "Continuous Softmax Attention" ("Analysis of the
