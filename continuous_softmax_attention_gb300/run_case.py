@@ -31,6 +31,8 @@ def main():
     ap.add_argument("--no-std", action="store_true")
     ap.add_argument("--decode", action="store_true")
     ap.add_argument("--backward", action="store_true")
+    ap.add_argument("--short-conv", action="store_true",
+                    help="the first-order (eq. (13)) form instead of the exact one")
     a = ap.parse_args()
     if a.decode:
         return run_decode(a)
@@ -40,7 +42,8 @@ def main():
     g = {k: v.cuda() for k, v in x.items()}
     scale = 1.0 / math.sqrt(a.d)
     for _ in range(a.iters):
-        o, lse = csa.forward(g["q"], g["k"], g["v"], g["k0"], g["v0"], mode=a.mode, scale=scale)
+        o, lse = csa.forward(g["q"], g["k"], g["v"], g["k0"], g["v0"], mode=a.mode, scale=scale,
+                             short_conv=a.short_conv)
         if not a.no_std:
             csa.std_forward(g["q"], g["k"], g["v"], scale=scale)
     torch.cuda.synchronize()
