@@ -13,6 +13,9 @@ What it computes follows Jianlin Su, "Continuous Softmax Attention"
 * ``forward_eq11``   - eq. (10)/(11), the softmax of ``a + b``.
 * ``forward_rows``   - eq. (8) for selected rows only (large shapes).
 * ``std_forward``    - eq. (12), standard causal softmax attention.
+* ``forward_symmetric`` - eq. (8) over the symmetric interval [1/2, t + 1/2]
+                       of the original Continuum Attention paper (constant
+                       end half-cells, no sink).
 * ``forward_short_conv`` - the short-conv reading of eq. (13): b replaced by
                        its first-order Taylor term (a cheaper variant).
 * ``row_bias``       - the logits ``a`` and corrections ``b`` of eq. (10)
@@ -76,6 +79,10 @@ def _load():
     lib.csa_oracle_forward_short_conv.restype = i
     lib.csa_oracle_forward_short_conv_rows.argtypes = [p, p, p, p, p, p, ll, p, p, i, i, i, i, d, i, i]
     lib.csa_oracle_forward_short_conv_rows.restype = i
+    lib.csa_oracle_forward_symmetric.argtypes = [p, p, p, p, p, i, i, i, i, d, i]
+    lib.csa_oracle_forward_symmetric.restype = i
+    lib.csa_oracle_forward_symmetric_rows.argtypes = [p, p, p, p, ll, p, p, i, i, i, i, d, i]
+    lib.csa_oracle_forward_symmetric_rows.restype = i
     lib.csa_oracle_log_dphi2.restype = d
     lib.csa_oracle_log_dphi2.argtypes = [d]
     lib.csa_oracle_backward.argtypes = [p, p, p, p, p, p, p, p, p, p, p, i, i, i, i, d, i, i]
@@ -186,6 +193,41 @@ def forward_short_conv_rows(q, k, v, rows, k0=None, v0=None, scale=None, mode=ZE
     rc = _load().csa_oracle_forward_short_conv_rows(
         _ptr(q), _ptr(k), _ptr(v), _ptr(k0), _ptr(v0), _ptr(rows), n, _ptr(out), _ptr(lse), B, H,
         T, d, float(scale), int(mode), int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return out, lse
+
+
+def forward_symmetric(q, k, v, scale=None, nthreads=None):
+    """eq. (8) over the symmetric interval [1/2, t + 1/2] (constant end
+    half-cells, no sink).  Returns (o, lse)."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, H, T, d = _shape(q)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.zeros((B, H, T, d), dtype=np.float64)
+    lse = np.zeros((B, H, T), dtype=np.float64)
+    rc = _load().csa_oracle_forward_symmetric(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                              B, H, T, d, float(scale),
+                                              int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return out, lse
+
+
+def forward_symmetric_rows(q, k, v, rows, scale=None, nthreads=None):
+    """forward_symmetric for the flat rows given.  Returns (o[nrows, d], lse[nrows])."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, H, T, d = _shape(q)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = rows.shape[0]
+    out = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    rc = _load().csa_oracle_forward_symmetric_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(rows), n,
+                                                   _ptr(out), _ptr(lse), B, H, T, d, float(scale),
+                                                   int(nthreads or default_threads()))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
     return out, lse

@@ -102,7 +102,8 @@ typedef struct {
     /* explicit row list (NULL = all rows) */
     const long long *rows;
     long long nrows;
-    int form; /* 0 = eq.(8), 1 = eq.(11), 2 = eq.(12) standard, 3 = eq.(13) short conv */
+    int form; /* 0 = eq.(8), 1 = eq.(11), 2 = eq.(12) standard, 3 = eq.(13) short conv,
+               * 4 = eq.(8) over the symmetric interval [1/2, t + 1/2] */
 } job_t;
 
 typedef struct {
@@ -163,6 +164,38 @@ static void one_row(const job_t *jb, long long flat, double *out_row, double *ls
             const float *vi = val_ptr(jb, bh, i, h, zero);
             for (int c = 0; c < d; ++c) num[c] += w * (double)vi[c];
             den += w;
+        }
+        for (int c = 0; c < d; ++c) out_row[c] = num[c] / den;
+        if (lse_out) *lse_out = m + log(den);
+        return;
+    }
+
+    if (jb->form == 4) {
+        /* The symmetric interval [1/2, t + 1/2] of the original Continuum
+         * Attention paper ("Problem Statement"): eq. (2)'s integrals with
+         * eq. (3) inside [1, t] and constant half-cells [1/2, 1] (k_1, v_1)
+         * and [t, t + 1/2] (k_t, v_t), since a causal row has no k_{t+1}; no
+         * sink.  Segment i = 2..t contributes as in eq. (8); each half-cell
+         * contributes e^{a} v / 2 and e^{a} / 2. */
+        const int t = r + 1;
+        double m = -INFINITY;
+        for (int i = 1; i <= t; ++i) {
+            a[i] = jb->scale * dot_fd(key_ptr(jb, bh, i, h, zero), qd, d);
+            if (a[i] > m) m = a[i];
+        }
+        const float *v1 = val_ptr(jb, bh, 1, h, zero), *vt = val_ptr(jb, bh, t, h, zero);
+        const double h1 = 0.5 * exp(a[1] - m), ht = 0.5 * exp(a[t] - m);
+        double den = h1 + ht;
+        for (int c = 0; c < d; ++c) num[c] = h1 * (double)v1[c] + ht * (double)vt[c];
+        for (int i = 2; i <= t; ++i) {
+            const double delta = a[i] - a[i - 1];
+            const double e1 = exp(a[i - 1] - m + csa_oracle_log_phi1(delta));
+            const double e2 = exp(a[i - 1] - m + csa_oracle_log_phi2(delta));
+            const float *vi = val_ptr(jb, bh, i, h, zero);
+            const float *vp = val_ptr(jb, bh, i - 1, h, zero);
+            for (int c = 0; c < d; ++c)
+                num[c] += e1 * (double)vi[c] + e2 * ((double)vp[c] - (double)vi[c]);
+            den += e1;
         }
         for (int c = 0; c < d; ++c) out_row[c] = num[c] / den;
         if (lse_out) *lse_out = m + log(den);
@@ -403,6 +436,24 @@ int csa_oracle_forward_short_conv_rows(const float *q, const float *k, const flo
 {
     if (!rows && nrows > 0) return -1;
     return forward_common(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, rows, nrows, 3, nthreads);
+}
+
+/* eq.(8) over the symmetric interval [1/2, t + 1/2], no sink. */
+int csa_oracle_forward_symmetric(const float *q, const float *k, const float *v, double *out,
+                                 double *lse, int B, int H, int T, int d, double scale,
+                                 int nthreads)
+{
+    return forward_common(q, k, v, NULL, NULL, out, lse, B, H, T, d, scale, 0, NULL, 0, 4, nthreads);
+}
+
+/* The symmetric interval for a list of rows only. */
+int csa_oracle_forward_symmetric_rows(const float *q, const float *k, const float *v,
+                                      const long long *rows, long long nrows, double *out,
+                                      double *lse, int B, int H, int T, int d, double scale,
+                                      int nthreads)
+{
+    if (!rows && nrows > 0) return -1;
+    return forward_common(q, k, v, NULL, NULL, out, lse, B, H, T, d, scale, 0, rows, nrows, 4, nthreads);
 }
 
 /* Standard causal softmax attention, eq.(12). */

@@ -87,3 +87,55 @@ def forward(q, k, v, k0=None, v0=None, scale=None, mode=ZERO, nodes=20):
                 out[b, h, r] = (e[:, None] * vv).sum(axis=0) / den
                 lse[b, h, r] = m + math.log(den)
     return out, lse
+
+
+def forward_symmetric(q, k, v, scale=None, nodes=20):
+    """The symmetric interval of the original Continuum Attention paper (cited
+    in "Problem Statement"): eq. (2)'s integrals over [1/2, t + 1/2] instead of
+    [0, t].  Inside [1, t], k_s and v_s follow eq. (3); the end half-cells
+    [1/2, 1] and [t, t + 1/2] hold k_1, v_1 and k_t, v_t constant (a causal
+    row has no k_{t+1}), so no sink is needed.  By quadrature, as forward()."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, T, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    xg, wg = np.polynomial.legendre.leggauss(nodes)
+    xi_unit = 0.5 * (xg + 1.0)
+    w_unit = 0.5 * wg
+    out = np.zeros((B, H, T, d))
+    lse = np.zeros((B, H, T))
+    for b in range(B):
+        for h in range(H):
+            K, V = k[b, h], v[b, h]  # row j is the page's key j + 1
+            for r in range(T):
+                t = r + 1
+                qt = q[b, h, r]
+                pts_logit, pts_val, pts_w = [], [], []
+                # half-cells: a constant integrand over a length of 1/2 each
+                for j in {0, t - 1}:
+                    pts_logit.append(np.full(nodes, scale * (K[j] @ qt)))
+                    pts_val.append(np.tile(V[j], (nodes, 1)))
+                    pts_w.append(w_unit * (0.5 if t > 1 else 1.0))
+                # eq. (3) on the unit intervals [i-1, i], i = 2..t (page keys)
+                for i in range(2, t + 1):
+                    a0, a1 = K[i - 2], K[i - 1]
+                    delta = scale * (qt @ (a1 - a0))
+                    pieces = max(1, int(math.ceil(abs(delta) / 2.0)))
+                    for p in range(pieces):
+                        s_loc = (p + xi_unit) / pieces
+                        ks = np.outer(1.0 - s_loc, a0) + np.outer(s_loc, a1)
+                        vs = np.outer(1.0 - s_loc, V[i - 2]) + np.outer(s_loc, V[i - 1])
+                        pts_logit.append(scale * (ks @ qt))
+                        pts_val.append(vs)
+                        pts_w.append(w_unit / pieces)
+                lg = np.concatenate(pts_logit)
+                vv = np.concatenate(pts_val)
+                ww = np.concatenate(pts_w)
+                m = lg.max()
+                e = ww * np.exp(lg - m)
+                den = e.sum()
+                out[b, h, r] = (e[:, None] * vv).sum(axis=0) / den
+                lse[b, h, r] = m + math.log(den)
+    return out, lse
