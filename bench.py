@@ -218,6 +218,7 @@ def run_gpu(args):
     csa_call = lambda: csa.forward(g["q"], g["k"], g["v"], mode=w.modes[0], scale=scale, out=out, lse=lse)
     sc_call = lambda: csa.forward(g["q"], g["k"], g["v"], mode=w.modes[0], scale=scale, out=out,
                                   lse=lse, short_conv=True)
+    sym_call = lambda: csa.forward_symmetric(g["q"], g["k"], g["v"], scale=scale, out=out, lse=lse)
     std_call = lambda: csa.std_forward(g["q"], g["k"], g["v"], scale=scale, out=out, lse=lse)
 
     dec = None if args.no_decode else DecodeBench(csa, dev, stream, flush)
@@ -244,6 +245,7 @@ def run_gpu(args):
         csa_call()
         std_call()
         sc_call()
+        sym_call()
         e2e_call()
         if dec is not None:
             dec.call()
@@ -259,6 +261,7 @@ def run_gpu(args):
         ms_csa = timed(csa_call, args.steps)
         ms_std = timed(std_call, args.steps)
         ms_sc = timed(sc_call, args.steps)
+        ms_sym = timed(sym_call, args.steps)
         ms_e2e = timed(e2e_call, args.steps)
         if dec is not None:
             dec.ms = timed(dec.call, args.decode_steps)
@@ -274,6 +277,7 @@ def run_gpu(args):
 
     tot_csa, tot_std, tot_e2e = total(ms_csa), total(ms_std), total(ms_e2e)
     tot_sc = total(ms_sc)
+    tot_sym = total(ms_sym)
     if ws > 1:
         dist.destroy_process_group()
     if rank != 0:
@@ -312,7 +316,11 @@ def run_gpu(args):
                        "ms_per_step": round(tot_sc / K, 5),
                        "ratio_over_std": round((flops / tot_sc) / (flops_std / tot_std), 4),
                        "note": "first-order (eq. (13)) reading of the same step, csa_forward_short_conv"},
-        "gpu_launches": 4 * K + (0 if dec is None else 2 * 2 * args.decode_steps) +
+        "symmetric": {"value": round(ws * flops_std * K / (tot_sym * 1e-3) / 1e12, 3),
+                      "unit": UNIT, "ms_per_step": round(tot_sym / K, 5),
+                      "note": "eq. (2) over [1/2, t+1/2] (csa_forward_symmetric); flops over its "
+                              "B*H*T(T+1)/2 pairs (no sink)"},
+        "gpu_launches": 5 * K + (0 if dec is None else 2 * 2 * args.decode_steps) +
                         (0 if bwd is None else bwd.launches * args.backward_steps),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": burst,
                      "unit": "TFLOP/s", "frac": round(achieved / burst, 4),

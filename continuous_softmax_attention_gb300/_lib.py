@@ -51,6 +51,7 @@ def load():
     for name, args in (("csa_forward", fwd), ("csa_forward_f32", fwd),
                        ("csa_forward_short_conv", fwd), ("csa_forward_short_conv_f32", fwd),
                        ("csa_std_forward", std), ("csa_std_forward_f32", std),
+                       ("csa_forward_symmetric", std), ("csa_forward_symmetric_f32", std),
                        ("csa_logphi2_eval", [p, p, i, p]),
                        ("csa_segment_weights_eval", [p, p, p, p, i, p]),
                        ("csa_device_status", []),
@@ -157,7 +158,8 @@ def forward(q, k, v, k0=None, v0=None, *, mode: int = 0, scale=None, out=None, l
     return out, lse
 
 
-def std_forward(q, k, v, *, scale=None, out=None, lse=None, stream=None, want_lse: bool = True):
+def std_forward(q, k, v, *, scale=None, out=None, lse=None, stream=None, want_lse: bool = True,
+                _entry: str = "csa_std_forward"):
     """Standard causal softmax attention (b = 0, no sink).  Returns (o, lse)."""
     import torch
 
@@ -175,15 +177,21 @@ def std_forward(q, k, v, *, scale=None, out=None, lse=None, stream=None, want_ls
     if lse is not None:
         _check_tensor(lse, "lse", torch.float32, (B, H, T), dev)
     lib = load()
-    if dtype == torch.bfloat16:
-        fn, where = lib.csa_std_forward, "csa_std_forward"
-    elif dtype == torch.float32:
-        fn, where = lib.csa_std_forward_f32, "csa_std_forward_f32"
-    else:
+    if dtype not in (torch.bfloat16, torch.float32):
         raise ValueError(f"unsupported dtype {dtype}")
+    where = _entry + ("" if dtype == torch.bfloat16 else "_f32")
+    fn = getattr(lib, where)
     _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, T, d, float(scale),
               _stream_handle(stream)), where)
     return out, lse
+
+
+def forward_symmetric(q, k, v, *, scale=None, out=None, lse=None, stream=None,
+                      want_lse: bool = True):
+    """Continuous attention over the symmetric interval [1/2, t + 1/2]
+    (constant end half-cells, no sink).  Returns (o, lse)."""
+    return std_forward(q, k, v, scale=scale, out=out, lse=lse, stream=stream, want_lse=want_lse,
+                       _entry="csa_forward_symmetric")
 
 
 def decode_workspace_bytes(B: int, H: int, T: int, d: int) -> int:

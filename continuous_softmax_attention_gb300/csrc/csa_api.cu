@@ -224,6 +224,19 @@ int csa_forward_short_conv(const void *q, const void *k, const void *v, const vo
                         stream);
 }
 
+int csa_forward_symmetric(const void *q, const void *k, const void *v, void *out, float *lse,
+                          int B, int H, int T, int d, float scale, csa_stream_t stream) {
+    return forward_bf16(q, k, v, nullptr, nullptr, out, lse, B, H, T, d, scale, CSA_K0_ZERO,
+                        kFormSymmetric, stream);
+}
+
+int csa_forward_symmetric_f32(const float *q, const float *k, const float *v, float *out,
+                              float *lse, int B, int H, int T, int d, float scale,
+                              csa_stream_t stream) {
+    return forward_f32(q, k, v, nullptr, nullptr, out, lse, B, H, T, d, scale, CSA_K0_ZERO,
+                       kFormSymmetric, stream);
+}
+
 int csa_forward_short_conv_f32(const float *q, const float *k, const float *v, const float *k0,
                                const float *v0, float *out, float *lse, int B, int H, int T,
                                int d, float scale, int k0_mode, csa_stream_t stream) {

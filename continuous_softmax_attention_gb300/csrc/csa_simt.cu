@@ -134,7 +134,8 @@ struct RowIO {
 };
 
 // grid: one warp per (b, h, row); rows handed out longest first.
-// FORM: 0 eq. (10)/(11), 1 the short-conv reading of eq. (13), 2 eq. (12).
+// FORM: 0 eq. (10)/(11), 1 the short-conv reading of eq. (13), 2 eq. (12),
+// 3 the symmetric interval [1/2, t + 1/2] (constant end half-cells, no sink).
 template <typename Tin, int NPL, int FORM>
 __global__ void __launch_bounds__(256) simt_forward_kernel(const Tin *q, const Tin *k,
                                                            const Tin *v, const Tin *k0,
@@ -167,7 +168,20 @@ __global__ void __launch_bounds__(256) simt_forward_kernel(const Tin *q, const T
         float a_next = io.logit(io.key(1), scale);
         for (int i = 0; i <= t; ++i) {
             float b;
-            if (FORM == 1) {
+            if (FORM == 3) {
+                // e^{b_i} = (i == 1 ? 1/2 : phi2(a_{i-1} - a_i)) + (i == t ? 1/2 : phi2(a_{i+1} - a_i));
+                // the sink takes no part
+                constexpr float kLogHalf = -0.69314718055994531f;
+                if (i == 0) {
+                    a_prev = a_cur;
+                    a_cur = a_next;
+                    if (i + 2 <= t) a_next = io.logit(io.key(i + 2), scale);
+                    continue;
+                }
+                const float lb = i == 1 ? kLogHalf : log_phi2_f32(a_prev - a_cur);
+                const float rb = i == t ? kLogHalf : log_phi2_f32(a_next - a_cur);
+                b = logaddexp_f32(lb, rb);
+            } else if (FORM == 1) {
                 // log phi2(x) = -log 2 + x/3 + ..; log(phi2(x) + phi2(y)) = (x + y)/6 + ..
                 constexpr float kLn2f = 0.69314718055994531f;
                 if (i == 0)
@@ -244,6 +258,8 @@ cudaError_t csa_simt_forward_f32(const float *q, const float *k, const float *v,
         return launch_any<float, 0>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
     if (form == 1)
         return launch_any<float, 1>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
+    if (form == 3)
+        return launch_any<float, 3>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, 0, stream);
     return launch_any<float, 2>(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, stream);
 }
 
@@ -260,6 +276,8 @@ cudaError_t csa_simt_forward_bf16(const void *q, const void *k, const void *v, c
         return launch_any<bf, 0>(q_, k_, v_, k0_, v0_, o_, lse, B, H, T, d, scale, mode, stream);
     if (form == 1)
         return launch_any<bf, 1>(q_, k_, v_, k0_, v0_, o_, lse, B, H, T, d, scale, mode, stream);
+    if (form == 3)
+        return launch_any<bf, 3>(q_, k_, v_, k0_, v0_, o_, lse, B, H, T, d, scale, 0, stream);
     return launch_any<bf, 2>(q_, k_, v_, k0_, v0_, o_, lse, B, H, T, d, scale, mode, stream);
 }
 

@@ -41,7 +41,9 @@
 // The template flag SHORT turns the kernel into the short-conv reading of
 // eq. (13): b is replaced by its first-order term, so a key's weight is
 // 2^z with z an affine combination of its own and its neighbours' logits
-// (short_chunk) and no phi2 is formed.
+// (short_chunk) and no phi2 is formed.  SYM integrates over the symmetric
+// interval [1/2, t + 1/2] instead (constant half-cells at both ends, no
+// sink; cont_chunk).
 //
 // The two column halves of a row exchange their partial maxima, the L share
 // that crosses into the next tile, and their final sums through shared
@@ -157,9 +159,15 @@ __device__ __forceinline__ void seg_weights(float X, float p0, float p1, float &
 // columns cbase..cbase+32; Lc is the L share of column cbase coming from the
 // left.  Produces w[0..31] (e^{a+b-m} * (ln2)^2), returns in Lc the L share
 // of column cbase+32, and in L31 that of cbase+31.
-template <bool MASKED>
+// SYM, the symmetric interval [1/2, t + 1/2] with constant end half-cells:
+// with first_cell (the chunk holding the sink and key 1) the sink takes no
+// weight and key 1's left share is its half-cell p_1/2; each row's last key
+// (MASKED) adds its right half-cell p/2 (both times (ln 2)^2).
+template <bool MASKED, bool SYM>
 __device__ __forceinline__ void cont_chunk(const float (&sv)[33], float k2, float nm, int cbase,
-                                           int c_last, float &Lc, float &L31, float (&w)[32]) {
+                                           int c_last, bool first_cell, float &Lc, float &L31,
+                                           float (&w)[32]) {
+    constexpr float kHalfCell = 0.5f * kLn2 * kLn2;
     float u[33], pe[33], L[33], R[32];
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
@@ -182,6 +190,10 @@ __device__ __forceinline__ void cont_chunk(const float (&sv)[33], float k2, floa
             Ri = seg_ok ? Ri : 0.0f;
             Li = seg_ok ? Li : 0.0f;
         }
+        if (SYM && i == 0 && first_cell) {
+            Ri = 0.0f;                    // the sink is not part of [1/2, t + 1/2]
+            Li = kHalfCell * pe[1];       // key 1's left half-cell
+        }
         R[i] = Ri;
         L[i + 1] = Li;
     }
@@ -190,6 +202,11 @@ __device__ __forceinline__ void cont_chunk(const float (&sv)[33], float k2, floa
         const float2 t = __fadd2_rn(make_float2(L[i], L[i + 1]), make_float2(R[i], R[i + 1]));
         w[i] = t.x;
         w[i + 1] = t.y;
+    }
+    if (SYM && MASKED) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            w[i] = cbase + i == c_last ? fmaf(kHalfCell, pe[i], w[i]) : w[i];  // right half-cell
     }
     L31 = L[31];
     Lc = L[32];
@@ -282,7 +299,7 @@ __device__ __forceinline__ uint32_t p_col(int k) { return k < 2 ? 16u * k : 80u 
 // half's first key (for half 0 of the first tile: none, the sink is an end);
 // out (half 1), that of column 126, the left neighbour of the next tile's
 // first key.  tile0: this is the first key tile (column 0 is the sink).
-template <bool MASKED, bool SHORT>
+template <bool MASKED, bool SHORT, bool SYM>
 __device__ __forceinline__ void half_weights(uint32_t tS, const uint32_t (&a)[2][32], uint32_t nb,
                                              RowState &st, int half, int c_last, int sink,
                                              bool tile0, float nm, float &Lc) {
@@ -315,7 +332,7 @@ __device__ __forceinline__ void half_weights(uint32_t tS, const uint32_t (&a)[2]
             L31 = sv[30];  // column 126 when k == 3
             Lc = sv[31];   // left neighbour of the next chunk
         } else {
-            cont_chunk<MASKED>(sv, k2, nm, 32 * k, c_last, Lc, L31, w);
+            cont_chunk<MASKED, SYM>(sv, k2, nm, 32 * k, c_last, k == 0 && tile0, Lc, L31, w);
         }
         if (k == 3) {
             Lc = L31;  // carried to the next tile's first key
@@ -346,7 +363,7 @@ __device__ __forceinline__ void half_weights(uint32_t tS, const uint32_t (&a)[2]
     st.l_run += lsum.x + lsum.y;
 }
 
-template <int D, bool SHORT>
+template <int D, bool SHORT, bool SYM>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_forward_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -571,6 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float s0 = __uint_as_float(a[0][0]);
             if (half == 0 && sink == 1) s0 = __uint_as_float(a[0][1]);
             if (half == 0 && sink == 2) s0 = st.s_sink;
+            // the symmetric interval has no sink: its logit must not raise the max
+            if (SYM && half == 0 && j == 0) s0 = -INFINITY;
             const float mine = masked ? half_max<true>(a, half, c_last, s0)
                                       : half_max<false>(a, half, c_last, s0);
             // exchange the partial maxima (and the carried L share) with the other half
@@ -595,9 +614,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float nm = -st.m_run;
             if (masked)
-                half_weights<true, SHORT>(tS, a, nb[0], st, half, c_last, sink, j == 0, nm, Lc);
+                half_weights<true, SHORT, SYM>(tS, a, nb[0], st, half, c_last, sink, j == 0, nm, Lc);
             else
-                half_weights<false, SHORT>(tS, a, nb[0], st, half, c_last, sink, j == 0, nm, Lc);
+                half_weights<false, SHORT, SYM>(tS, a, nb[0], st, half, c_last, sink, j == 0, nm, Lc);
             if (half == 1) xcarry[(xe & 1) * 128 + irow] = Lc;
             // Rescale O (this half's value columns; half 1 also the row-sum
             // column) when the max moved, after PV(j-1) finished.
@@ -721,7 +740,7 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns) {
 }
 
 // ---------------------------------------------------------------- host side
-template <int D, bool SHORT>
+template <int D, bool SHORT, bool SYM>
 int launch_tc(const void *q, const void *k, const void *v, const void *k0, const void *v0,
               void *out, float *lse, int B, int H, int T, float scale, int mode,
               cudaStream_t stream) {
@@ -745,7 +764,7 @@ int launch_tc(const void *q, const void *k, const void *v, const void *k0, const
     prm.lse = lse;
     const long long grid = (long long)prm.num_qtiles * BH;
     if (grid > 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
-    auto kern = tc_forward_kernel<D, SHORT>;
+    auto kern = tc_forward_kernel<D, SHORT, SYM>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return CSA_ERR_CUDA;
@@ -758,12 +777,21 @@ int launch_tc(const void *q, const void *k, const void *v, const void *k0, const
 int csa_tc_forward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
                    void *out, float *lse, int B, int H, int T, int d, float scale, int mode,
                    int form, cudaStream_t stream) {
-    const bool sc = form == kFormShortConv;
-    if (d == 128 && !sc) return launch_tc<128, false>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
-    if (d == 64 && !sc) return launch_tc<64, false>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
-    if (d == 128) return launch_tc<128, true>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
-    if (d == 64) return launch_tc<64, true>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream);
-    return CSA_ERR_UNSUPPORTED;
+#define CSA_TC_LAUNCH(DD, SC, SY) \
+    return launch_tc<DD, SC, SY>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream)
+    if (d != 64 && d != 128) return CSA_ERR_UNSUPPORTED;
+    if (form == kFormShortConv) {
+        if (d == 128) CSA_TC_LAUNCH(128, true, false);
+        CSA_TC_LAUNCH(64, true, false);
+    }
+    if (form == kFormSymmetric) {  // no sink: mode is ignored
+        mode = CSA_K0_ZERO;
+        if (d == 128) CSA_TC_LAUNCH(128, false, true);
+        CSA_TC_LAUNCH(64, false, true);
+    }
+    if (d == 128) CSA_TC_LAUNCH(128, false, false);
+    CSA_TC_LAUNCH(64, false, false);
+#undef CSA_TC_LAUNCH
 }
 
 cudaError_t csa_tc_segment_weights_eval(const float *u0, const float *u1, float *right,

@@ -125,6 +125,27 @@ int csa_forward_short_conv_f32(const float *q, const float *k, const float *v, c
                                int d, float scale, int k0_mode, csa_stream_t stream);
 
 /*
+ * csa_forward_symmetric - continuous attention over the symmetric interval
+ *   [1/2, t + 1/2] that the original Continuum Attention paper uses (cited in
+ *   "Problem Statement" of "Continuous Softmax Attention"; eq. (2) with that
+ *   interval).  Inside [1, t] keys and values follow eq. (3); the end
+ *   half-cells [1/2, 1] and [t, t + 1/2] hold k_1, v_1 and k_t, v_t constant
+ *   (a causal row has no k_{t+1}), so there is no sink.  As weights:
+ *       e^{b_{t,1}} = 1/2 + phi2(a_{t,2} - a_{t,1}),
+ *       e^{b_{t,t}} = phi2(a_{t,t-1} - a_{t,t}) + 1/2,
+ *       interior keys as eq. (10); t = 1 gives o_1 = v_1.
+ *   lse_t = log of the denominator integral over [1/2, t + 1/2].  bf16; same
+ *   layout, alignment and d rules as csa_forward (no k0, v0, mode).
+ */
+int csa_forward_symmetric(const void *q, const void *k, const void *v, void *out, float *lse,
+                          int B, int H, int T, int d, float scale, csa_stream_t stream);
+
+/* csa_forward_symmetric_f32 - the same in fp32 on CUDA cores, 1 <= d <= 256. */
+int csa_forward_symmetric_f32(const float *q, const float *k, const float *v, float *out,
+                              float *lse, int B, int H, int T, int d, float scale,
+                              csa_stream_t stream);
+
+/*
  * csa_std_forward - standard causal softmax attention (b = 0, no sink),
  *   bf16 inputs, tensor-core path.
  *   Defines: eq. (12) of "Continuous Softmax Attention" ("Analysis of the
