@@ -82,3 +82,83 @@ def max_over_ranks(value: float, device=None, group=None) -> float:
     t = torch.tensor([float(value)], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
     return float(t.item())
+
+
+def backward_sharded(q, k, v, out, lse, dout, k0=None, v0=None, *, mode: int = 0, scale=None,
+                     gather=True, group=None, fn=None):
+    """The backward pass on this rank's share of the (b, h) problems.
+
+    fn(q, k, v, out, lse, dout, k0, v0, mode=, scale=) -> (dq, dk, dv, dk0,
+    dv0) computes one shard (the CUDA kernel, continuous_softmax_attention_
+    gb300.backward, by default).  dq, dk, dv need no exchange; the gradients
+    of the per-head sink pair (mode GIVEN) sum over the whole batch, so each
+    rank's partial [H, d] sums are all-reduced.  Returns (dq, dk, dv, dk0,
+    dv0) for the full problem when gather is true, else this rank's dq, dk,
+    dv shard with the all-reduced dk0, dv0 and its [start, stop) range."""
+    world = dist.get_world_size(group) if dist.is_initialized() else 1
+    rank = dist.get_rank(group) if dist.is_initialized() else 0
+    if fn is None:
+        from . import backward as fn
+    B, H, T, d = q.shape
+    start, stop = head_shard(B * H, world, rank)
+    flat = lambda t: t.reshape(B * H, T, d)[start:stop].unsqueeze(0).contiguous()
+    lse_s = lse.reshape(B * H, T)[start:stop].unsqueeze(0).contiguous()
+    heads = torch.arange(start, stop, device=q.device) % H
+    k0s = k0.index_select(0, heads) if (k0 is not None and mode == 2) else None
+    v0s = v0.index_select(0, heads) if (v0 is not None and mode == 2) else None
+    dq, dk, dv, dk0_s, dv0_s = fn(flat(q), flat(k), flat(v), flat(out), lse_s, flat(dout), k0s,
+                                  v0s, mode=mode, scale=scale)
+    dk0 = dv0 = None
+    if mode == 2:
+        # the shard's problems are [1, n] with head ids `heads`: fold its
+        # per-problem sink gradients back onto the H heads, then sum ranks
+        dk0 = torch.zeros((H, d), dtype=torch.float64, device=q.device)
+        dv0 = torch.zeros((H, d), dtype=torch.float64, device=q.device)
+        dk0.index_add_(0, heads, dk0_s.to(torch.float64))
+        dv0.index_add_(0, heads, dv0_s.to(torch.float64))
+        if world > 1:
+            dist.all_reduce(dk0, group=group)
+            dist.all_reduce(dv0, group=group)
+    if not gather:
+        return dq, dk, dv, dk0, dv0, (start, stop)
+    if world == 1:
+        return (dq.reshape(B, H, T, d), dk.reshape(B, H, T, d), dv.reshape(B, H, T, d), dk0, dv0)
+    lse_dummy = torch.zeros(dq.shape[:-1], dtype=torch.float32, device=q.device)
+    gq, _ = gather_outputs(dq, lse_dummy, B, H, world, group)
+    gk, _ = gather_outputs(dk, lse_dummy, B, H, world, group)
+    gv, _ = gather_outputs(dv, lse_dummy, B, H, world, group)
+    return gq, gk, gv, dk0, dv0
+
+
+def decode_sharded(q, k_cache, v_cache, k0=None, v0=None, *, seqlens=None, mode: int = 0,
+                   scale=None, gather=True, group=None, fn=None):
+    """A decode step on this rank's share of the sequences (whole sequences
+    per rank, so each keeps its own length).  fn(q, k, v, k0, v0, seqlens=,
+    mode=, scale=) -> (o, lse) computes one shard (the CUDA decode step by
+    default).  No collective on the data path; gather=True all-gathers the
+    per-sequence outputs."""
+    world = dist.get_world_size(group) if dist.is_initialized() else 1
+    rank = dist.get_rank(group) if dist.is_initialized() else 0
+    if fn is None:
+        from . import decode as fn
+    B = k_cache.shape[0]
+    start, stop = head_shard(B, world, rank)
+    sl = None if seqlens is None else seqlens[start:stop].contiguous()
+    o, lse = fn(q[start:stop].contiguous(), k_cache[start:stop].contiguous(),
+                v_cache[start:stop].contiguous(), k0, v0, seqlens=sl, mode=mode, scale=scale)
+    if not gather or world == 1:
+        return (o, lse) if gather else (o, lse, (start, stop))
+    H, d = q.shape[1], q.shape[2]
+    width = max(b - a for a, b in (head_shard(B, world, r) for r in range(world)))
+    pad_o = torch.zeros((width, H, d), dtype=o.dtype, device=o.device)
+    pad_l = torch.zeros((width, H), dtype=lse.dtype, device=lse.device)
+    pad_o[:stop - start] = o
+    pad_l[:stop - start] = lse
+    go = [torch.empty_like(pad_o) for _ in range(world)]
+    gl = [torch.empty_like(pad_l) for _ in range(world)]
+    dist.all_gather(go, pad_o, group=group)
+    dist.all_gather(gl, pad_l, group=group)
+    sizes = [head_shard(B, world, r) for r in range(world)]
+    o_full = torch.cat([go[r][: b - a] for r, (a, b) in enumerate(sizes)])
+    l_full = torch.cat([gl[r][: b - a] for r, (a, b) in enumerate(sizes)])
+    return o_full, l_full

@@ -89,3 +89,122 @@ def test_single_process_path():
                              fn=_oracle_fn)
     assert o.shape == (1, 2, 10, 4) and lse.shape == (1, 2, 10)
     assert max_over_ranks(3.5) == 3.5
+
+
+def _oracle_bwd(q, k, v, out, lse, dout, k0, v0, mode, scale):
+    import oracle
+
+    r = oracle.backward(q, k, v, dout, k0, v0, scale=scale, mode=mode, nthreads=1)
+    t = lambda a: None if a is None else torch.from_numpy(a)
+    return t(r["dq"]), t(r["dk"]), t(r["dv"]), t(r["dk0"]), t(r["dv0"])
+
+
+def _bwd_worker(rank, world, port, B, H, T, d, mode, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from continuous_softmax_attention_gb300.dist import backward_sharded
+        from continuous_softmax_attention_gb300.inputs import make_inputs
+
+        x = make_inputs(B, H, T, d, "f32", seed=43)
+        g = torch.randn(B, H, T, d, generator=torch.Generator().manual_seed(2))
+        lse = torch.zeros(B, H, T)
+        res = backward_sharded(x["q"], x["k"], x["v"], x["q"], lse, g, x["k0"], x["v0"],
+                               mode=mode, scale=0.5, fn=_oracle_bwd)
+        if rank == 0:
+            q.put(tuple(None if t is None else t.numpy() for t in res))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("B,H,mode", [(2, 3, 2), (1, 3, 0), (3, 1, 1)])
+def test_backward_two_gloo_ranks(B, H, mode):
+    """dq, dk, dv shard with no exchange; the sink gradients (mode GIVEN) are
+    all-reduced across ranks; everything matches one process."""
+    import oracle
+    from continuous_softmax_attention_gb300.inputs import make_inputs
+
+    T, d, world = 12, 4, 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_bwd_worker, args=(r, world, port, B, H, T, d, mode, q))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    dq, dk, dv, dk0, dv0 = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    x = make_inputs(B, H, T, d, "f32", seed=43)
+    g = torch.randn(B, H, T, d, generator=torch.Generator().manual_seed(2))
+    ref = oracle.backward(x["q"], x["k"], x["v"], g, x["k0"], x["v0"], scale=0.5, mode=mode)
+    assert np.array_equal(dq, ref["dq"]) and np.array_equal(dk, ref["dk"])
+    assert np.array_equal(dv, ref["dv"])
+    if mode == 2:
+        assert np.abs(dk0 - ref["dk0"]).max() < 1e-12 and np.abs(dv0 - ref["dv0"]).max() < 1e-12
+    else:
+        assert dk0 is None and dv0 is None
+
+
+def _oracle_decode(q, k, v, k0, v0, seqlens, mode, scale):
+    """Row n_b - 1 of eq. (8) for every (b, h): the decode result."""
+    import oracle
+
+    B, H, T, d = k.shape
+    o = torch.zeros(B, H, d, dtype=torch.float64)
+    lse = torch.zeros(B, H, dtype=torch.float64)
+    for b in range(B):
+        n = int(seqlens[b])
+        qf = torch.zeros(1, H, n, d)
+        qf[0, :, n - 1] = q[b]
+        ro, rl = oracle.forward_rows(qf, k[b:b + 1, :, :n], v[b:b + 1, :, :n],
+                                     oracle.flat_rows(1, H, n, [(0, h, n - 1) for h in range(H)]),
+                                     k0, v0, scale=scale, mode=mode, nthreads=1)
+        o[b] = torch.from_numpy(ro)
+        lse[b] = torch.from_numpy(rl)
+    return o, lse
+
+
+def _dec_worker(rank, world, port, mode, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from continuous_softmax_attention_gb300.dist import decode_sharded
+        from continuous_softmax_attention_gb300.inputs import make_decode_inputs
+
+        x = make_decode_inputs(5, 2, 30, 8, seed=8, len_lo=1)
+        o, lse = decode_sharded(x["q"].float(), x["k"].float(), x["v"].float(), x["k0"].float(),
+                                x["v0"].float(), seqlens=x["seqlens"], mode=mode, scale=0.4,
+                                fn=lambda *a, seqlens, mode, scale: _oracle_decode(
+                                    *a, seqlens, mode, scale))
+        if rank == 0:
+            q.put((o.numpy(), lse.numpy()))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("mode", [0, 2])
+def test_decode_two_gloo_ranks(mode):
+    """Whole sequences per rank, no collective on the data path; the gathered
+    step equals one process's."""
+    from continuous_softmax_attention_gb300.inputs import make_decode_inputs
+
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_dec_worker, args=(r, 2, port, mode, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    o, lse = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    x = make_decode_inputs(5, 2, 30, 8, seed=8, len_lo=1)
+    ro, rl = _oracle_decode(x["q"].float(), x["k"].float(), x["v"].float(), x["k0"].float(),
+                            x["v0"].float(), x["seqlens"], mode, 0.4)
+    assert np.array_equal(o, ro.numpy()) and np.array_equal(lse, rl.numpy())
