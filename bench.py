@@ -337,6 +337,12 @@ def run_gpu(args):
         line["backward"] = bwd.summary(ws, args.backward_steps, max_over_ranks, dev, burst, src)
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = cpu_baseline(x, scale, budget_s=args.cpu_seconds)
+        line["short_conv"]["cpu_baseline"] = cpu_baseline_form(x, scale, "short_conv")
+        line["symmetric"]["cpu_baseline"] = cpu_baseline_form(x, scale, "symmetric")
+        if bwd is not None:
+            line["backward"]["cpu_baseline"] = cpu_baseline_backward(x, scale, w.modes[0])
+        if dec is not None:
+            line["decode"]["cpu_baseline"] = cpu_baseline_decode(dec)
     return line
 
 
@@ -406,6 +412,7 @@ class DecodeBench:
         self.w = w = DECODE_WORKLOADS["decode"]
         x = decode_workload_inputs("decode")
         self.lens = x["seqlens"].tolist()
+        self.host = x
         self.bytes = decode_bytes(self.lens, w.H, w.d)
         g = {k: t.to(dev) for k, t in x.items()}
         self.q, self.k, self.v, self.sl = g["q"], g["k"], g["v"], g["seqlens"]
@@ -508,6 +515,88 @@ def cpu_baseline(x, scale, budget_s=15.0, seed=0):
             "sample": f"{len(picks)} rows drawn uniformly from the {B}x{H}x{T}x{d} workload "
                       f"(eq. (8) in double, {dt:.1f} s)",
             "seconds": round(dt, 3)}
+
+
+def cpu_baseline_form(x, scale, form, budget_s=4.0, seed=1):
+    """The oracle of the short-conv or symmetric form on rows sampled from the
+    workload (double, all host cores); rate = algorithmic flops / wall time."""
+    import oracle
+
+    B, H, T, d = x["q"].shape
+    q, k, v = (x[n].float().numpy() for n in ("q", "k", "v"))
+    cores = oracle.default_threads()
+    fn = oracle.forward_short_conv_rows if form == "short_conv" else oracle.forward_symmetric_rows
+    per_row = (lambda r: r + 2) if form == "short_conv" else (lambda r: r + 1)
+    n = 16 * cores
+    while True:
+        picks = _sample_rows(T, H, n, seed)
+        rows = oracle.flat_rows(B, H, T, picks)
+        t0 = time.perf_counter()
+        fn(q, k, v, rows, scale=scale, nthreads=cores)
+        dt = time.perf_counter() - t0
+        if dt > 0.25 * budget_s or n >= 1 << 20:
+            break
+        n = int(n * min(8.0, max(2.0, 0.5 * budget_s / max(dt, 1e-3))))
+    rate = 4.0 * d * sum(per_row(r) for (_, _, r) in picks) / dt / 1e12
+    return {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(picks)} rows drawn uniformly from the {B}x{H}x{T}x{d} workload "
+                      f"({form} form in double, {dt:.1f} s)",
+            "seconds": round(dt, 3)}
+
+
+def cpu_baseline_backward(x, scale, mode, T_sample=1024):
+    """The backward oracle (chain rule, double) on causal prefixes of one head
+    per host core (the heads run in parallel); rate = 10 d flops per pair /
+    wall time."""
+    import torch
+
+    import oracle
+
+    cores = oracle.default_threads()
+    B, H, T, d = x["q"].shape
+    hs = min(H, cores)
+    Ts = min(T, T_sample)
+    sl = lambda t: t[:, :hs, :Ts].contiguous()
+    g = torch.randn(1, hs, Ts, d, generator=torch.Generator().manual_seed(3))
+    t0 = time.perf_counter()
+    oracle.backward(sl(x["q"]), sl(x["k"]), sl(x["v"]), g, x["k0"][:hs], x["v0"][:hs],
+                    scale=scale, mode=mode, nthreads=cores)
+    dt = time.perf_counter() - t0
+    flops = 10.0 * d * hs * Ts * (Ts + 3) / 2
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": min(cores, hs), "kind": "oracle",
+            "sample": f"{hs} heads x the first {Ts} rows of the {B}x{H}x{T}x{d} workload "
+                      f"(chain rule in double, {dt:.1f} s)",
+            "seconds": round(dt, 3)}
+
+
+def cpu_baseline_decode(dec, budget_s=4.0):
+    """The oracle (eq. (8) row n_b of each sequence, double, all host cores)
+    on the decode workload's first sequences; rate = their cache bytes /
+    wall time."""
+    import torch
+
+    import oracle
+
+    cores = oracle.default_threads()
+    x, w = dec.host, dec.w
+    done, nbytes, t_all = 0, 0, 0.0
+    while done < w.B and t_all < budget_s:
+        n = dec.lens[done]
+        qf = torch.zeros(1, w.H, n, w.d)
+        qf[0, :, n - 1] = x["q"][done].float()
+        rows = oracle.flat_rows(1, w.H, n, [(0, h, n - 1) for h in range(w.H)])
+        t0 = time.perf_counter()
+        oracle.forward_rows(qf, x["k"][done:done + 1, :, :n], x["v"][done:done + 1, :, :n], rows,
+                            scale=1.0 / math.sqrt(w.d), nthreads=cores)
+        t_all += time.perf_counter() - t0
+        nbytes += 2 * n * w.H * w.d * 2
+        done += 1
+    return {"value": round(nbytes / t_all / 1e9, 3), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"the first {done} of {w.B} sequences, all {w.H} heads (eq. (8) row n_b "
+                      f"in double, {t_all:.1f} s; the conversion of the cache to float32 is not "
+                      f"timed)",
+            "seconds": round(t_all, 3)}
 
 
 def run_reference(args):

@@ -156,3 +156,13 @@ def test_backward_tensor_core_matches_cuda_core_path():
         check(b, ref[name], "bf16", "cuda-core " + name)
         diff = (a.float() - b.float()).abs().max().item()
         assert diff <= 2e-2 * np.abs(ref[name]).max(), (name, diff)
+
+
+@pytest.mark.parametrize("T,d,mode", [(2048, 128, 2), (4096, 64, 0)])
+def test_backward_long_rows(T, d, mode):
+    """Rows of 2048 and 4096 keys: 17 and 33 key tiles per head, the lazy
+    statistics of many query tiles, on two heads (the oracle runs them in
+    parallel, a few seconds each)."""
+    x = make_inputs(1, 2, T, d, "bf16", seed=190 + T)
+    g = upstream((1, 2, T, d), 13)
+    compare(x, g, 1.0 / d ** 0.5, mode, "bf16", f"long T={T} d={d}")
