@@ -15,6 +15,8 @@ from ._lib import (  # noqa: F401
     decode_workspace_bytes,
     device_status,
     forward,
+    forward_host,
+    forward_host_workspace_bytes,
     forward_symmetric,
     logphi2_eval,
     segment_weights_eval,
@@ -24,7 +26,8 @@ from ._lib import (  # noqa: F401
 )
 
 __all__ = [
-    "ZERO", "COPY_FIRST", "GIVEN", "CsaError", "forward", "forward_symmetric", "std_forward",
+    "ZERO", "COPY_FIRST", "GIVEN", "CsaError", "forward", "forward_host",
+    "forward_host_workspace_bytes", "forward_symmetric", "std_forward",
     "backward",
     "backward_workspace_bytes", "decode", "decode_noalloc", "decode_workspace_bytes", "logphi2_eval",
     "segment_weights_eval", "device_status", "selftest_wait_timeout", "status_string",

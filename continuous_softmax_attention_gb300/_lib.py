@@ -60,11 +60,14 @@ def load():
                        ("csa_decode", [p, p, p, p, p, p, p, p, p, ctypes.c_longlong, i, i, i, i,
                                        f, i, p]),
                        ("csa_decode_noalloc", [p, p, p, p, p, p, p, p, i, i, i, i, f, i, p]),
-                       ("csa_backward", bwd), ("csa_backward_f32", bwd)):
+                       ("csa_backward", bwd), ("csa_backward_f32", bwd),
+                       ("csa_forward_host", [p, p, p, p, p, p, p, p, ctypes.c_longlong, i, i, i,
+                                             i, f, i, i, p, p, p])):
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = i
-    for name in ("csa_decode_workspace_bytes", "csa_backward_workspace_bytes"):
+    for name in ("csa_decode_workspace_bytes", "csa_backward_workspace_bytes",
+                 "csa_forward_host_workspace_bytes"):
         getattr(lib, name).argtypes = [i, i, i, i]
         getattr(lib, name).restype = ctypes.c_longlong
     lib.csa_status_string.argtypes = [i]
@@ -155,6 +158,55 @@ def forward(q, k, v, k0=None, v0=None, *, mode: int = 0, scale=None, out=None, l
     fn = getattr(lib, where)
     _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(k0), _ptr(v0), _ptr(out), _ptr(lse),
               B, H, T, d, float(scale), int(mode), _stream_handle(stream)), where)
+    return out, lse
+
+
+def forward_host_workspace_bytes(B: int, H: int, T: int, d: int) -> int:
+    """Device workspace bytes csa_forward_host needs (host-side)."""
+    n = int(load().csa_forward_host_workspace_bytes(int(B), int(H), int(T), int(d)))
+    if n < 0:
+        raise CsaError(CSA_ERR_UNSUPPORTED, "csa_forward_host_workspace_bytes")
+    return n
+
+
+def forward_host(q, k, v, out, lse=None, k0=None, v0=None, *, mode: int = 0, scale=None,
+                 workspace=None, heads_per_chunk: int = 4, stream=None, stream_h2d=None,
+                 stream_d2h=None):
+    """csa_forward from host tensors, end to end, with the copies overlapped.
+
+    q, k, v, out: CPU bf16 [B, H, T, d] (pinned for the overlap); lse: CPU
+    float32 [B, H, T] or None; k0, v0: CUDA [H, d] in mode GIVEN.
+    workspace: CUDA uint8 tensor of forward_host_workspace_bytes(...) bytes.
+    The call is asynchronous: out and lse are ready once `stream` (torch's
+    current stream by default) has reached this point."""
+    import torch
+
+    B, H, T, d = q.shape
+    cpu = torch.device("cpu")
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _check_tensor(t, name, torch.bfloat16, (B, H, T, d), cpu)
+    if lse is not None:
+        _check_tensor(lse, "lse", torch.float32, (B, H, T), cpu)
+    if workspace is None or not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    dev = workspace.device
+    if mode == 2:
+        if k0 is None or v0 is None:
+            raise ValueError("mode 2 (given sink) needs k0 and v0")
+        _check_tensor(k0, "k0", torch.bfloat16, (H, d), dev)
+        _check_tensor(v0, "v0", torch.bfloat16, (H, d), dev)
+    else:
+        k0 = v0 = None
+    if scale is None:
+        scale = 1.0 / d ** 0.5
+    nbytes = workspace.numel() * workspace.element_size()
+    cs = _stream_handle(stream)
+    hs = _stream_handle(stream_h2d) if stream_h2d is not None else cs
+    ds = _stream_handle(stream_d2h) if stream_d2h is not None else cs
+    _check(load().csa_forward_host(_ptr(q), _ptr(k), _ptr(v), _ptr(k0), _ptr(v0), _ptr(out),
+                                   _ptr(lse), _ptr(workspace), nbytes, B, H, T, d, float(scale),
+                                   int(mode), int(heads_per_chunk), cs, hs, ds),
+           "csa_forward_host")
     return out, lse
 
 

@@ -199,6 +199,34 @@ int csa_backward_f32(const float *q, const float *k, const float *v, const float
                         workspace_bytes, B, H, T, d, scale, k0_mode, false, stream);
 }
 
+long long csa_forward_host_workspace_bytes(int B, int H, int T, int d) {
+    if (d > 256) return -1;
+    return csa_host_scratch_bytes(B, H, T, d);
+}
+
+int csa_forward_host(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+                     void *out, float *lse, void *workspace, long long workspace_bytes, int B,
+                     int H, int T, int d, float scale, int k0_mode, int heads_per_chunk,
+                     csa_stream_t stream, csa_stream_t stream_h2d, csa_stream_t stream_d2h) {
+    bool empty;
+    int rc = check_common(q, k, v, k0, v0, out, B, H, T, d, scale, k0_mode, true, &empty);
+    if (rc != CSA_OK || empty) return rc;
+    if (d > 256) return CSA_ERR_UNSUPPORTED;
+    if (heads_per_chunk < 1 || heads_per_chunk > H || H % heads_per_chunk != 0)
+        return CSA_ERR_INVALID_ARG;
+    if (!workspace) return CSA_ERR_INVALID_ARG;
+    const long long need = csa_host_scratch_bytes(B, H, T, d);
+    if (need < 0 || workspace_bytes < need) return CSA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256) || (lse && !aligned(lse, 4))) return CSA_ERR_ALIGNMENT;
+    if (k0_mode == CSA_K0_GIVEN && (!aligned(k0, 2) || !aligned(v0, 2))) return CSA_ERR_ALIGNMENT;
+    if ((d == 64 || d == 128) && scale < 0.0f) return CSA_ERR_UNSUPPORTED;
+    if ((rc = device_ok()) != CSA_OK) return rc;
+    return csa_host_forward(q, k, v, k0, v0, out, lse, workspace, B, H, T, d, scale, k0_mode,
+                            heads_per_chunk, reinterpret_cast<cudaStream_t>(stream),
+                            reinterpret_cast<cudaStream_t>(stream_h2d),
+                            reinterpret_cast<cudaStream_t>(stream_d2h));
+}
+
 long long csa_decode_workspace_bytes(int B, int H, int T, int d) {
     return csa_decode_scratch_bytes(B, H, T, d);
 }

@@ -103,6 +103,37 @@ int csa_forward_f32(const float *q, const float *k, const float *v, const float 
                     float scale, int k0_mode, csa_stream_t stream);
 
 /*
+ * csa_forward_host - csa_forward from HOST buffers, end to end: copies q, k,
+ *   v to the device, runs the forward pass and copies out and lse back,
+ *   overlapping the copies of one chunk of heads with the kernel of another
+ *   (the (b, h) problems are independent).  Same definition, result and
+ *   d rules as csa_forward.
+ *   q, k, v, out: HOST bf16 [B, H, T, d]; lse: HOST float [B, H, T] or NULL.
+ *   They should be page-locked (cudaHostAlloc / cudaHostRegister): pageable
+ *   memory is still correct but the copies then do not overlap.  The host
+ *   inputs must stay unchanged, and out/lse must not be read, until the work
+ *   completes on `stream`.
+ *   k0, v0: DEVICE bf16 [H, d] (CSA_K0_GIVEN only).
+ *   workspace: DEVICE scratch of at least csa_forward_host_workspace_bytes
+ *   (B, H, T, d) bytes, 256-byte aligned (device copies of q, k, v, out,
+ *   lse).
+ *   heads_per_chunk: heads per pipeline chunk; must divide H.
+ *   stream runs the kernels; stream_h2d and stream_d2h the two copy
+ *   directions (they may equal stream, at the cost of the overlap).  All
+ *   work of the call is complete once `stream` reaches the point after it.
+ *   Errors as csa_forward, plus CSA_ERR_INVALID_ARG for a heads_per_chunk
+ *   that does not divide H or a workspace too small.
+ */
+int csa_forward_host(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+                     void *out, float *lse, void *workspace, long long workspace_bytes, int B,
+                     int H, int T, int d, float scale, int k0_mode, int heads_per_chunk,
+                     csa_stream_t stream, csa_stream_t stream_h2d, csa_stream_t stream_d2h);
+
+/* csa_forward_host_workspace_bytes - device workspace csa_forward_host needs
+ * (host only), or -1 for a negative size or d outside 1..256. */
+long long csa_forward_host_workspace_bytes(int B, int H, int T, int d);
+
+/*
  * csa_forward_short_conv - the short-conv reading of eq. (13) ("Analysis of
  *   the Result" of "Continuous Softmax Attention"): the correction b is
  *   replaced by its first-order Taylor term, which the page likens to a
