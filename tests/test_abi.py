@@ -157,3 +157,24 @@ def test_backward_validation(lib):
 
     if not torch.cuda.is_available():
         assert bwd(lib, ws_bytes=need) == L.CSA_ERR_NO_DEVICE
+
+
+def test_forward_host_validation(lib):
+    need = lib.csa_forward_host_workspace_bytes(1, 4, 16, 64)
+    # q, k, v, out bf16 and lse fp32, each rounded up to 256 bytes
+    assert need == 4 * (4 * 16 * 64 * 2) + 256
+    call = lambda **kw: lib.csa_forward_host(
+        kw.get("q", FAKE), FAKE, FAKE, None, None, FAKE, None, kw.get("ws", ctypes.c_void_p(1 << 20)),
+        kw.get("ws_bytes", need), 1, 4, 16, 64, ctypes.c_float(0.1), 0, kw.get("hpc", 2), None,
+        None, None)
+    lib.csa_forward_host.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_longlong] + [ctypes.c_int] * 4 + \
+        [ctypes.c_float, ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 3
+    assert call(hpc=3) == L.CSA_ERR_INVALID_ARG  # does not divide H
+    assert call(hpc=0) == L.CSA_ERR_INVALID_ARG
+    assert call(ws_bytes=need - 1) == L.CSA_ERR_INVALID_ARG
+    assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == L.CSA_ERR_ALIGNMENT
+    assert call(q=NULL) == L.CSA_ERR_INVALID_ARG
+    import torch
+
+    if not torch.cuda.is_available():
+        assert call() == L.CSA_ERR_NO_DEVICE

@@ -175,3 +175,13 @@ def test_decode_argument_errors():
         decode(dev["q"], dev["k"], dev["v"], mode=2)
     o, lse = decode(dev["q"][:0], dev["k"][:0], dev["v"][:0])  # empty batch
     assert o.shape == (0, 1, 128)
+
+
+def test_decode_very_long_cache():
+    """One sequence of 131072 cached keys (1041 chunks) next to a short one."""
+    B, H, T, d = 2, 2, 131072, 128
+    x = make_decode_inputs(B, H, T, d, seed=510, len_lo=T)
+    lens = [T, 1000]
+    o, lse = run_decode(x, lens, None, 2)
+    ro, rl = oracle_decode(x, lens, 1.0 / d ** 0.5, 2, [(0, 0), (0, 1), (1, 0), (1, 1)])
+    check(o.reshape(-1, d), lse.reshape(-1), ro, rl, "T=131072")

@@ -78,3 +78,23 @@ def test_long_workload():
     """B=1, H=8, T=32768, d=64, given per-head k0, v0 (trainable-sink mode)."""
     w, x, g, o, lse, mode, scale = _run("long")
     _sampled(x, o, lse, mode, scale, rows_per_head=24, seed=4)
+
+
+def test_forward_very_long_rows():
+    """T = 131072 (1024 query tiles, 1033 key tiles per head): index and TMA
+    coordinate arithmetic at length, checked on the last rows and every few
+    thousandth row against the oracle."""
+    B, H, T, d = 1, 2, 131072, 64
+    from continuous_softmax_attention_gb300.inputs import make_inputs
+
+    x = make_inputs(B, H, T, d, "bf16", seed=500)
+    g = to_dev(x)
+    o, lse = csa.forward(g["q"], g["k"], g["v"], g["k0"], g["v0"], mode=2)
+    torch.cuda.synchronize()
+    rows = sorted(set([0, 1, 126, 127, 128, T - 129, T - 2, T - 1] + list(range(0, T, 9973))))
+    picks = [(0, h, r) for h in range(H) for r in rows]
+    flat = oracle.flat_rows(B, H, T, picks)
+    ro, rl = oracle.forward_rows(x["q"], x["k"], x["v"], flat, x["k0"], x["v0"],
+                                 scale=1.0 / d ** 0.5, mode=2)
+    idx = torch.as_tensor(flat)
+    assert_close(o.reshape(-1, d)[idx], lse.reshape(-1)[idx], ro, rl, "bf16", "T=131072")
