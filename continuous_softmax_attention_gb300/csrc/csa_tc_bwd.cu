@@ -26,7 +26,9 @@
 // memory with vector reductions.  Warps:
 //   0-7  elementwise: warp w owns TMEM lanes 32*(w%4).. and the column half
 //        w/4 (64 columns); they also run the dQ and final dK/dV epilogues
-//   8    TMA producer (the key tile once, then Q and dO per query tile)
+//   8    TMA producer (the key tile once, then Q and dO per query tile; Q
+//        double-buffered and fetched a tile ahead, dO as soon as dV has
+//        released its buffer)
 //   9    TMEM allocator and tcgen05.mma issuer
 // Tensor memory: S | dP (then dQ_part) | dV | dK.
 #include <cuda.h>
@@ -90,18 +92,21 @@ template <int D>
 struct BwCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kTileBytes = kChunks * kChunkBytes;  // [128 rows][D] bf16
-    static constexpr int kStages = D == 128 ? 1 : 2;          // Q + dO stages
+    static constexpr int kStagesQ = 2;                        // Q: fetched a tile ahead
+    static constexpr int kStagesG = D == 128 ? 1 : 2;         // dO
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kTileBytes;
-    static constexpr int kOffQ = kOffV + kTileBytes;             // [stage]
-    static constexpr int kOffG = kOffQ + kStages * kTileBytes;   // [stage] dO
-    static constexpr int kOffP = kOffG + kStages * kTileBytes;   // 2 boxes [128 q][64 keys]
+    static constexpr int kOffQ = kOffV + kTileBytes;              // [stage]
+    static constexpr int kOffG = kOffQ + kStagesQ * kTileBytes;   // [stage] dO
+    static constexpr int kOffP = kOffG + kStagesG * kTileBytes;   // 2 boxes [128 q][64 keys]
     static constexpr int kOffS = kOffP + 2 * kChunkBytes;        // dS, same layout
     static constexpr int kOffBar = kOffS + 2 * kChunkBytes;
     static constexpr int kBarKV = 0;
     static constexpr int kBarQFull = 1;
-    static constexpr int kBarQEmpty = kBarQFull + kStages;
-    static constexpr int kBarSFull = kBarQEmpty + kStages;  // S and dP in TMEM
+    static constexpr int kBarQEmpty = kBarQFull + kStagesQ;
+    static constexpr int kBarGFull = kBarQEmpty + kStagesQ;
+    static constexpr int kBarGEmpty = kBarGFull + kStagesG;
+    static constexpr int kBarSFull = kBarGEmpty + kStagesG;  // S and dP in TMEM
     static constexpr int kBarPReady = kBarSFull + 1;        // P, dS in shared memory
     static constexpr int kBarDqFull = kBarPReady + 1;       // dV, dK, dQ_part MMAs done
     static constexpr int kBarDqRead = kBarDqFull + 1;       // dQ_part read out of TMEM
@@ -109,6 +114,7 @@ struct BwCfg {
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
     static constexpr uint32_t kColS = 0;
     static constexpr uint32_t kColP = 128;
     static constexpr uint32_t kColV = 256;
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_g, const BwParams p) {
     using C = BwCfg<D>;
-    constexpr int NS = C::kStages;
+    constexpr int NQ = C::kStagesQ, NG = C::kStagesG;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -260,9 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(C::kBarKV), 1);
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < NQ; ++s) {
             mbar_init(BAR(C::kBarQFull + s), 1);
             mbar_init(BAR(C::kBarQEmpty + s), 1);
+        }
+        for (int s = 0; s < NG; ++s) {
+            mbar_init(BAR(C::kBarGFull + s), 1);
+            mbar_init(BAR(C::kBarGEmpty + s), 1);
         }
         mbar_init(BAR(C::kBarSFull), 1);
         mbar_init(BAR(C::kBarPReady), 256);
@@ -293,24 +303,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(sK + c * kChunkBytes, &tm_k, 64 * c, krow0, bh, BAR(C::kBarKV));
                 tma_load_3d(sV + c * kChunkBytes, &tm_v, 64 * c, krow0, bh, BAR(C::kBarKV));
             }
-            int issued = 0;
+            // Q of tile j goes out as soon as its stage is free (a tile ahead);
+            // dO of tile j once dV(j-1) has released its buffer.
+            int issued_q = 0, issued_g = 0;
             for (int j = 0; j < nQ; ++j) {
-                const int s = j % NS;
-                if (!wait_b(BAR(C::kBarQEmpty + s), ((j / NS) & 1) ^ 1, abort_flag)) break;
                 const int qrow = 128 * (q_first + j);
-                mbar_arrive_expect_tx(BAR(C::kBarQFull + s), 2 * C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(sQ + s * C::kTileBytes + c * kChunkBytes, &tm_q, 64 * c, qrow, bh,
-                                BAR(C::kBarQFull + s));
-                    tma_load_3d(sG + s * C::kTileBytes + c * kChunkBytes, &tm_g, 64 * c, qrow, bh,
-                                BAR(C::kBarQFull + s));
-                }
-                issued = j + 1;
+                const int sq = j % NQ, sg = j % NG;
+                if (!wait_b(BAR(C::kBarQEmpty + sq), ((j / NQ) & 1) ^ 1, abort_flag)) break;
+                mbar_arrive_expect_tx(BAR(C::kBarQFull + sq), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(sQ + sq * C::kTileBytes + c * kChunkBytes, &tm_q, 64 * c, qrow, bh,
+                                BAR(C::kBarQFull + sq));
+                issued_q = j + 1;
+                if (!wait_b(BAR(C::kBarGEmpty + sg), ((j / NG) & 1) ^ 1, abort_flag)) break;
+                mbar_arrive_expect_tx(BAR(C::kBarGFull + sg), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(sG + sg * C::kTileBytes + c * kChunkBytes, &tm_g, 64 * c, qrow, bh,
+                                BAR(C::kBarGFull + sg));
+                issued_g = j + 1;
             }
             // Let every copy this thread issued land before the block can exit.
             wait_bar_drain(BAR(C::kBarKV), 0, &g_bwd_status);
-            for (int j = max(0, issued - NS); j < issued; ++j)
-                wait_bar_drain(BAR(C::kBarQFull + j % NS), (j / NS) & 1, &g_bwd_status);
+            for (int j = max(0, issued_q - NQ); j < issued_q; ++j)
+                wait_bar_drain(BAR(C::kBarQFull + j % NQ), (j / NQ) & 1, &g_bwd_status);
+            for (int j = max(0, issued_g - NG); j < issued_g; ++j)
+                wait_bar_drain(BAR(C::kBarGFull + j % NG), (j / NG) & 1, &g_bwd_status);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
@@ -345,9 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             for (int j = 0; ok && j < nQ; ++j) {
-                const int s = j % NS;
-                const uint32_t qb = sQ + s * C::kTileBytes, gb = sG + s * C::kTileBytes;
-                if (!(ok = wait_b(BAR(C::kBarQFull + s), (j / NS) & 1, abort_flag))) break;
+                const int sq = j % NQ, sg = j % NG;
+                const uint32_t qb = sQ + sq * C::kTileBytes, gb = sG + sg * C::kTileBytes;
+                if (!(ok = wait_b(BAR(C::kBarQFull + sq), (j / NQ) & 1, abort_flag))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -357,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // dP overwrites the dQ_part columns of the previous tile
                 if (j > 0 && !(ok = wait_b(BAR(C::kBarDqRead), (j - 1) & 1, abort_flag))) break;
+                if (!(ok = wait_b(BAR(C::kBarGFull + sg), (j / NG) & 1, abort_flag))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -370,14 +388,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // dV += P^T dO and dK += dS^T Q: A = P^T / dS^T, MN-major (keys
                 // contiguous, two 64-key boxes); B = dO / Q, MN-major; the
                 // reduction runs over the 128 query rows, 16 per step.
+                // dV first: once it completes, dO's buffer takes the next tile
+                // while dK and dQ run
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                for (int kk = 0; kk < 8; ++kk)
                     tc_mma_ss(tmem + C::kColV, make_sdesc(sP + kk * 2048, kChunkBytes, 1024),
-                              make_sdesc(gb + kk * 2048, kChunkBytes, 1024), kIdKV, acc);
+                              make_sdesc(gb + kk * 2048, kChunkBytes, 1024), kIdKV,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(BAR(C::kBarGEmpty + sg));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
                     tc_mma_ss(tmem + C::kColK, make_sdesc(sS + kk * 2048, kChunkBytes, 1024),
-                              make_sdesc(qb + kk * 2048, kChunkBytes, 1024), kIdKV, acc);
-                }
+                              make_sdesc(qb + kk * 2048, kChunkBytes, 1024), kIdKV,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(BAR(C::kBarQEmpty + sq));
                 // dQ_part = dS K: A = dS K-major (reduction over the 128 keys),
                 // B = the key tile, MN-major
 #pragma unroll
@@ -387,7 +411,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                               make_sdesc(sK + kk * 2048, kChunkBytes, 1024), kIdQ, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(BAR(C::kBarDqFull));
-                tc_commit(BAR(C::kBarQEmpty + s));
             }
             // every MMA this thread issued completes before the block exits
             tc_commit(BAR(C::kBarDrain));
