@@ -21,15 +21,19 @@
 // 128B-swizzled layout that serves as the MN-major A operand of
 // dV += P^T dO and dK += dS^T Q and as the K-major A operand of
 // dQ_part = dS K.  dV and dK accumulate in TMEM over the whole walk; dQ_part
-// goes to TMEM (in the dP columns, so that the next S product need not wait
-// for it to be read) and is added to an fp32 dq accumulator in global
-// memory with vector reductions.  Warps:
+// goes to TMEM (in the dP columns), is staged in fp32 where P and dS were
+// once the MMAs reading them are done, and is added to an fp32 dq
+// accumulator in global memory by TMA tensor reductions.  Per query tile the
+// tensor core runs dP(j), then dV(j), dQ_part(j), dK(j) and S(j+1): the
+// elementwise warps wait for one product chain per tile, not two.  Warps:
 //   0-7  elementwise: warp w owns TMEM lanes 32*(w%4).. and the column half
-//        w/4 (64 columns); they also run the dQ and final dK/dV epilogues
+//        w/4 (64 columns); they also stage dQ_part and run the final dK/dV
+//        epilogue
 //   8    TMA producer (the key tile once, then Q and dO per query tile; Q
 //        double-buffered and fetched a tile ahead, dO as soon as dV has
 //        released its buffer)
 //   9    TMEM allocator and tcgen05.mma issuer
+//   10   dQ reducer (TMA reductions of the staged dQ_part)
 // Tensor memory: S | dP (then dQ_part) | dV | dK.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -50,7 +54,8 @@ __device__ int g_bwd_status;  // sticky status word of this file's kernels
 
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
-constexpr int kThreads = 32 * 10;
+constexpr int kWarpReduce = 10;
+constexpr int kThreads = 32 * 11;
 constexpr int kKeyStride = 126;  // owned keys per key tile
 
 // tcgen05.mma kind::f16 instruction descriptor with the major-ness of A and
@@ -82,11 +87,23 @@ __device__ __forceinline__ void wait_ld17(uint32_t (&r)[16], uint32_t &x) {
                  : "memory");
 }
 
-__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
-                 : "memory");
+// Tiled 3-D TMA reduction: adds one fp32 box from shared memory into global
+// memory (elements outside the tensor are skipped).
+__device__ __forceinline__ void tma_reduce_add_3d(uint32_t src, const void *desc, int c0, int c1,
+                                                  int c2) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+        " [%0, {%1, %2, %3}], [%4];" ::"l"(reinterpret_cast<uint64_t>(desc)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(src)
+        : "memory");
 }
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of every committed reduction have been read
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// every committed reduction has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int D>
 struct BwCfg {
@@ -108,13 +125,18 @@ struct BwCfg {
     static constexpr int kBarGEmpty = kBarGFull + kStagesG;
     static constexpr int kBarSFull = kBarGEmpty + kStagesG;  // S and dP in TMEM
     static constexpr int kBarPReady = kBarSFull + 1;        // P, dS in shared memory
-    static constexpr int kBarDqFull = kBarPReady + 1;       // dV, dK, dQ_part MMAs done
+    static constexpr int kBarDqFull = kBarPReady + 1;       // dV, dQ_part MMAs done
     static constexpr int kBarDqRead = kBarDqFull + 1;       // dQ_part read out of TMEM
-    static constexpr int kBarDrain = kBarDqRead + 1;
+    static constexpr int kBarPFree = kBarDqRead + 1;       // dK done: P, dS no longer read
+    static constexpr int kBarStageFull = kBarPFree + 1;    // dQ_part staged (fp32) in P, dS
+    static constexpr int kBarStageFree = kBarStageFull + 1; // its reduction has read it
+    static constexpr int kBarDrain = kBarStageFree + 1;
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
     static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
+    // the fp32 dQ_part, boxes of [128 rows][32 columns], fits where P and dS were
+    static_assert(D / 32 * kChunkBytes <= 4 * kChunkBytes, "dQ staging");
     static constexpr uint32_t kColS = 0;
     static constexpr uint32_t kColP = 128;
     static constexpr uint32_t kColV = 256;
@@ -129,13 +151,41 @@ struct BwParams {
     int mode;
     const __nv_bfloat16 *k0, *v0;
     const float *lse, *Drow;  // [B*H*T]
-    float *dq_acc;            // [B*H*T*D]
     __nv_bfloat16 *dk, *dv;
     float *dk0, *dv0;
 };
 
+// mbarrier.try_wait with a suspend-time hint: a thread whose phase is not yet
+// complete sleeps until it completes (or the hint elapses) instead of
+// returning at once, so waiting roles take no issue slots from the
+// elementwise warps that share their scheduler.
+constexpr uint32_t kSuspendHintNs = 100000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait (2 s), as wait_bar, on the sleeping try_wait.
 __device__ __forceinline__ bool wait_b(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
-    return wait_bar(bar, parity, abort_flag, &g_bwd_status);
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            *(volatile int *)&g_bwd_status = kStatusTimeout;
+            __threadfence();
+            return false;
+        }
+    }
 }
 
 // One interval between a left key at u0 and a right key at u1 (log2 units,
@@ -236,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_backward_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
-                       const __grid_constant__ CUtensorMap tm_g, const BwParams p) {
+                       const __grid_constant__ CUtensorMap tm_g,
+                       const __grid_constant__ CUtensorMap tm_dq, const BwParams p) {
     using C = BwCfg<D>;
     constexpr int NQ = C::kStagesQ, NG = C::kStagesG;
     extern __shared__ uint8_t smem_raw[];
@@ -278,6 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(BAR(C::kBarPReady), 256);
         mbar_init(BAR(C::kBarDqFull), 1);
         mbar_init(BAR(C::kBarDqRead), 256);
+        mbar_init(BAR(C::kBarPFree), 1);
+        mbar_init(BAR(C::kBarStageFull), 256);
+        mbar_init(BAR(C::kBarStageFree), 1);
         mbar_init(BAR(C::kBarDrain), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -361,17 +415,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
             }
             tc_fence_after();
-            for (int j = 0; ok && j < nQ; ++j) {
-                const int sq = j % NQ, sg = j % NG;
-                const uint32_t qb = sQ + sq * C::kTileBytes, gb = sG + sg * C::kTileBytes;
-                if (!(ok = wait_b(BAR(C::kBarQFull + sq), (j / NQ) & 1, abort_flag))) break;
-                tc_fence_after();
+            // Per query tile j, in issue order: dP(j); then, once P and dS are
+            // ready, dV(j) (frees dO's buffer), dQ_part(j) (read out while the
+            // rest runs), dK(j) (frees Q's stage and the P, dS buffers), and
+            // S(j+1) into the S columns the elementwise warps have finished with.
+            auto issue_s = [&](uint32_t qb) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
                     tc_mma_ss(tmem + C::kColS, make_sdesc(qb + off, 16, 1024),
                               make_sdesc(sK + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
                 }
+            };
+            if (ok && (ok = wait_b(BAR(C::kBarQFull), 0, abort_flag))) {
+                tc_fence_after();
+                issue_s(sQ);
+            }
+            for (int j = 0; ok && j < nQ; ++j) {
+                const int sq = j % NQ, sg = j % NG;
+                const uint32_t qb = sQ + sq * C::kTileBytes, gb = sG + sg * C::kTileBytes;
                 // dP overwrites the dQ_part columns of the previous tile
                 if (j > 0 && !(ok = wait_b(BAR(C::kBarDqRead), (j - 1) & 1, abort_flag))) break;
                 if (!(ok = wait_b(BAR(C::kBarGFull + sg), (j / NG) & 1, abort_flag))) break;
@@ -388,20 +450,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // dV += P^T dO and dK += dS^T Q: A = P^T / dS^T, MN-major (keys
                 // contiguous, two 64-key boxes); B = dO / Q, MN-major; the
                 // reduction runs over the 128 query rows, 16 per step.
-                // dV first: once it completes, dO's buffer takes the next tile
-                // while dK and dQ run
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     tc_mma_ss(tmem + C::kColV, make_sdesc(sP + kk * 2048, kChunkBytes, 1024),
                               make_sdesc(gb + kk * 2048, kChunkBytes, 1024), kIdKV,
                               (j > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(BAR(C::kBarGEmpty + sg));
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_ss(tmem + C::kColK, make_sdesc(sS + kk * 2048, kChunkBytes, 1024),
-                              make_sdesc(qb + kk * 2048, kChunkBytes, 1024), kIdKV,
-                              (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(BAR(C::kBarQEmpty + sq));
                 // dQ_part = dS K: A = dS K-major (reduction over the 128 keys),
                 // B = the key tile, MN-major
 #pragma unroll
@@ -411,10 +465,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                               make_sdesc(sK + kk * 2048, kChunkBytes, 1024), kIdQ, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(BAR(C::kBarDqFull));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_ss(tmem + C::kColK, make_sdesc(sS + kk * 2048, kChunkBytes, 1024),
+                              make_sdesc(qb + kk * 2048, kChunkBytes, 1024), kIdKV,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(BAR(C::kBarQEmpty + sq));
+                tc_commit(BAR(C::kBarPFree));
+                if (j + 1 < nQ) {
+                    const int sq1 = (j + 1) % NQ;
+                    if (!(ok = wait_b(BAR(C::kBarQFull + sq1), ((j + 1) / NQ) & 1, abort_flag))) break;
+                    tc_fence_after();
+                    issue_s(sQ + sq1 * C::kTileBytes);
+                }
             }
             // every MMA this thread issued completes before the block exits
             tc_commit(BAR(C::kBarDrain));
             wait_bar_drain(BAR(C::kBarDrain), 0, &g_bwd_status);
+        }
+        __syncwarp();
+    } else if (warp == kWarpReduce) {
+        // ------------------------------------------------------ dQ reducer
+        // Adds each query tile's staged dQ_part into the fp32 accumulator
+        // with TMA reductions and frees the staging area once they have read it.
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_dq);
+            for (int j = 0; j < nQ; ++j) {
+                if (!wait_b(BAR(C::kBarStageFull), j & 1, abort_flag)) break;
+                const int row0 = 128 * (q_first + j);
+#pragma unroll
+                for (int b = 0; b < D / 32; ++b)
+                    tma_reduce_add_3d(sP + b * kChunkBytes, &tm_dq, 32 * b, row0, bh);
+                bulk_commit();
+                bulk_wait_read_all();
+                mbar_arrive(BAR(C::kBarStageFree));
+            }
+            bulk_wait_all();
         }
         __syncwarp();
     } else {
@@ -472,6 +558,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             // flight while chunk kk is computed
             uint32_t a[16], g[16], an[1] = {0u}, gn[1] = {0u};
             const int cb = 64 * half;
+            // this row's 16 keys from column c0 = 16-byte chunks ch, ch+1 of box c0/64
+            auto store_pds = [&](int c0, const uint32_t (&qP)[8], const uint32_t (&qS)[8]) {
+                const int box = c0 >> 6, ch = (c0 & 63) >> 3;
+                uint8_t *prow = smem + C::kOffP + box * kChunkBytes + irow * 128;
+                uint8_t *srow = smem + C::kOffS + box * kChunkBytes + irow * 128;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int pos = ((ch + h2) ^ (irow & 7)) << 4;
+                    *reinterpret_cast<uint4 *>(prow + pos) =
+                        make_uint4(qP[4 * h2], qP[4 * h2 + 1], qP[4 * h2 + 2], qP[4 * h2 + 3]);
+                    *reinterpret_cast<uint4 *>(srow + pos) =
+                        make_uint4(qS[4 * h2], qS[4 * h2 + 1], qS[4 * h2 + 2], qS[4 * h2 + 3]);
+                }
+            };
             tmem_ld16(tS + cb, a);
             tmem_ld16(tD + cb, g);
             tmem_ld1(tS + cb + 16, an[0]);
@@ -505,46 +605,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     cols16<false>(sv, gv, k2, lse2, Dr, scale, c0, c_last, zero_c0, last_chunk,
                                   Lc, Fc, pP, pS);
-                // this row's 16 keys = 16-byte chunks ch, ch+1 of box c0/64
-                const int box = c0 >> 6, ch = (c0 & 63) >> 3;
-                uint8_t *prow = smem + C::kOffP + box * kChunkBytes + irow * 128;
-                uint8_t *srow = smem + C::kOffS + box * kChunkBytes + irow * 128;
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int pos = ((ch + h2) ^ (irow & 7)) << 4;
-                    *reinterpret_cast<uint4 *>(prow + pos) =
-                        make_uint4(pP[4 * h2], pP[4 * h2 + 1], pP[4 * h2 + 2], pP[4 * h2 + 3]);
-                    *reinterpret_cast<uint4 *>(srow + pos) =
-                        make_uint4(pS[4 * h2], pS[4 * h2 + 1], pS[4 * h2 + 2], pS[4 * h2 + 3]);
+                if (kk == 0 && j > 0 &&
+                    !__all_sync(0xffffffffu, wait_b(BAR(C::kBarStageFree), (j - 1) & 1, abort_flag))) {
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");  // chunk 1's loads
+                    ok = false;
+                    break;
                 }
+                store_pds(c0, pP, pS);
             }
+            if (!ok) break;
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(BAR(C::kBarPReady));
-            // dQ_part of this query tile (in the dP columns), added into the
-            // fp32 accumulator
+            // dQ_part of this query tile (in the dP columns): out of TMEM, which
+            // frees the dP columns, then staged in fp32 where P and dS were (the
+            // MMAs that read them are complete), 128B-swizzled boxes of
+            // [128 rows][32 columns] for the reducer warp's TMA reductions
             ok = __all_sync(0xffffffffu, wait_b(BAR(C::kBarDqFull), j & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            float *dst = p.dq_acc + ((size_t)bh * T + (size_t)(rvalid ? r : 0)) * D + half * (D / 2);
+            uint32_t o[D / 64][32];
 #pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc) {
-                uint32_t o[32];
-                tmem_ld32(tD + half * (D / 2) + 32 * cc, o);
-                tmem_wait_ld_regs<32>(o);
-                if (rvalid) {
+            for (int cc = 0; cc < D / 64; ++cc) tmem_ld32(tD + half * (D / 2) + 32 * cc, o[cc]);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        red_add_v4(dst + 32 * cc + e, __uint_as_float(o[e]), __uint_as_float(o[e + 1]),
-                                   __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
-                }
-            }
+            for (int cc = 0; cc < D / 64; ++cc) tmem_wait_ld_regs<32>(o[cc]);
             tc_fence_before();
             mbar_arrive(BAR(C::kBarDqRead));
+            // the staging area is free once dK, the last MMA reading P and dS, is done
+            ok = __all_sync(0xffffffffu, wait_b(BAR(C::kBarPFree), j & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
+                uint8_t *srow = smem + C::kOffP + (half * (D / 64) + cc) * kChunkBytes + irow * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(srow + ((c ^ (irow & 7)) << 4)) =
+                        make_uint4(o[cc][4 * c], o[cc][4 * c + 1], o[cc][4 * c + 2], o[cc][4 * c + 3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(BAR(C::kBarStageFull));
         }
         if (ok) {
             // dV, dK of this tile's keys: TMEM lane = key row of the tile.
-            // The last DqFull wait covers every MMA of the walk.
+            // The last PFree wait covers every MMA of the walk.
             const int c = irow;
             const int arow = krow0 + c;
             const bool own = c >= 1 && c <= kKeyStride && arow < T;
@@ -627,6 +731,21 @@ __global__ void to_bf16_kernel(const float *a, __nv_bfloat16 *out, long long n4)
     reinterpret_cast<uint2 *>(out)[i] = pk;
 }
 
+// The fp32 dq accumulator [B*H, T, D] viewed as {D, T, B*H}, boxes of 32
+// columns x 128 rows (128 bytes per row, 128B swizzle); rows outside [0, T)
+// of a head are skipped by the reductions.
+bool encode_acc_map(CUtensorMap *map, float *ptr, int BH, int T, int D) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)T * D * 4};
+    const cuuint32_t box[3] = {32, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 int launch_bwd(const void *q, const void *k, const void *v, const void *k0, const void *v0,
                const void *o, const float *lse, const void *dout, void *dq, void *dk, void *dv,
@@ -637,9 +756,10 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *k0, cons
     const long long rows = (long long)BH * T;
     float *dq_acc = static_cast<float *>(scratch);
     float *Drow = dq_acc + rows * D;
-    CUtensorMap mq, mk, mv, mg;
+    CUtensorMap mq, mk, mv, mg, mdq;
     if (!encode_qkv_map(&mq, q, BH, T, D) || !encode_qkv_map(&mk, k, BH, T, D) ||
-        !encode_qkv_map(&mv, v, BH, T, D) || !encode_qkv_map(&mg, dout, BH, T, D))
+        !encode_qkv_map(&mv, v, BH, T, D) || !encode_qkv_map(&mg, dout, BH, T, D) ||
+        !encode_acc_map(&mdq, dq_acc, BH, T, D))
         return CSA_ERR_CUDA;
     if (cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)rows * D, stream) != cudaSuccess)
         return CSA_ERR_CUDA;
@@ -664,7 +784,6 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *k0, cons
     prm.v0 = static_cast<const __nv_bfloat16 *>(v0);
     prm.lse = lse;
     prm.Drow = Drow;
-    prm.dq_acc = dq_acc;
     prm.dk = static_cast<__nv_bfloat16 *>(dk);
     prm.dv = static_cast<__nv_bfloat16 *>(dv);
     prm.dk0 = dk0;
@@ -675,7 +794,7 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *k0, cons
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return CSA_ERR_CUDA;
-    kern<<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mg, prm);
+    kern<<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mg, mdq, prm);
     const long long n4 = rows * D / 4;
     to_bf16_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, stream>>>(
         dq_acc, static_cast<__nv_bfloat16 *>(dq), n4);
