@@ -24,8 +24,9 @@
 // goes to TMEM (in the dP columns), is staged in fp32 where P and dS were
 // once the MMAs reading them are done, and is added to an fp32 dq
 // accumulator in global memory by TMA tensor reductions.  Per query tile the
-// tensor core runs dP(j), then dV(j), dQ_part(j), dK(j) and S(j+1): the
-// elementwise warps wait for one product chain per tile, not two.  Warps:
+// tensor core runs dP(j), S(j+1) as soon as S(j) and dP(j) have been read
+// out of TMEM, then dV(j), dQ_part(j) and dK(j): after writing P and dS the
+// elementwise warps wait for four products, not five.  Warps:
 //   0-7  elementwise: warp w owns TMEM lanes 32*(w%4).. and the column half
 //        w/4 (64 columns); they also stage dQ_part and run the final dK/dV
 //        epilogue
@@ -124,7 +125,8 @@ struct BwCfg {
     static constexpr int kBarGFull = kBarQEmpty + kStagesQ;
     static constexpr int kBarGEmpty = kBarGFull + kStagesG;
     static constexpr int kBarSFull = kBarGEmpty + kStagesG;  // S and dP in TMEM
-    static constexpr int kBarPReady = kBarSFull + 1;        // P, dS in shared memory
+    static constexpr int kBarSRead = kBarSFull + 1;         // S and dP read out of TMEM
+    static constexpr int kBarPReady = kBarSRead + 1;        // P, dS in shared memory
     static constexpr int kBarDqFull = kBarPReady + 1;       // dV, dQ_part MMAs done
     static constexpr int kBarDqRead = kBarDqFull + 1;       // dQ_part read out of TMEM
     static constexpr int kBarPFree = kBarDqRead + 1;       // dK done: P, dS no longer read
@@ -195,32 +197,28 @@ __device__ __forceinline__ bool wait_b(uint32_t bar, uint32_t parity, volatile i
 //     R = (s - p0)/x,  L = s - R,  k = (s - 2R)/x,
 // using phi2' = (phi1 - 2 phi2)/x and identity (7).  The independent
 // rounding of p0 and p1 (2^-22 each) grows by up to 24/|x|^3 in k, so
-// |x| < 0.35 takes the power series of the integral definitions instead,
-//     phi2 = sum x^n/(n+2)!,  phi1 - phi2 = sum (n+1) x^n/(n+2)!,
-//     phi2' = sum (n+1) x^n/(n+3)!,
-// to degree 3, all times p0.  Both sides of the switch stay below 3e-4
-// relative error, under the 2^-9 rounding of the bf16 P and dS.
+// |x| < 0.35 takes series about the interval's midpoint instead: with
+// h = x/2 and sig = p0 + p1 (= 2 e^c cosh h, c the mid logit),
+//     s = sig tanh(h)/(2h)               = sig (1/2 - h^2/6 + ...),
+//     k = sig (h cosh h - sinh h)/(4 h^3 cosh h) = sig (1/12 - h^2/30 + ...),
+//     R = s/2 - h k,  L = s/2 + h k      (L - R = x k),
+// even in h, so one term beyond the constant is enough: both sides of the
+// switch stay below 2e-4 relative error, under the 2^-9 rounding of the
+// bf16 P and dS.
 __device__ __forceinline__ void interval(float u0, float u1, float p0, float p1, float &R,
                                          float &L, float &k) {
-    const float x = (u1 - u0) * kLn2;
-    float f2 = 1.0f / 120.0f, f12 = 1.0f / 30.0f, f3 = 1.0f / 180.0f;
-    f2 = fmaf(f2, x, 1.0f / 24.0f);
-    f12 = fmaf(f12, x, 1.0f / 8.0f);
-    f3 = fmaf(f3, x, 1.0f / 40.0f);
-    f2 = fmaf(f2, x, 1.0f / 6.0f);
-    f12 = fmaf(f12, x, 1.0f / 3.0f);
-    f3 = fmaf(f3, x, 1.0f / 12.0f);
-    f2 = fmaf(f2, x, 0.5f);
-    f12 = fmaf(f12, x, 0.5f);
-    f3 = fmaf(f3, x, 1.0f / 6.0f);
-    const float rx = rcp_approx(x);
+    const float h = (u1 - u0) * (0.5f * kLn2);
+    const float rx = rcp_approx(h + h);
     const float s = (p1 - p0) * rx;
     const float Rc = (s - p0) * rx;
     const float kc = fmaf(-2.0f, Rc, s) * rx;
-    const bool small = fabsf(x) < 0.35f;
-    R = small ? p0 * f2 : Rc;
-    L = small ? p0 * f12 : s - Rc;
-    k = small ? p0 * f3 : kc;
+    const float sig = p0 + p1, hh = h * h;
+    const float hs = sig * fmaf(hh, -1.0f / 12.0f, 0.25f);      // s/2
+    const float ks = sig * fmaf(hh, -1.0f / 30.0f, 1.0f / 12.0f);
+    const bool small = fabsf(h) < 0.175f;
+    R = small ? fmaf(-h, ks, hs) : Rc;
+    L = small ? fmaf(h, ks, hs) : s - Rc;
+    k = small ? ks : kc;
 }
 
 // 16 columns [c0, c0+16) of this row: P and dS, given the raw logits sv[]
@@ -326,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(C::kBarGEmpty + s), 1);
         }
         mbar_init(BAR(C::kBarSFull), 1);
+        mbar_init(BAR(C::kBarSRead), 256);
         mbar_init(BAR(C::kBarPReady), 256);
         mbar_init(BAR(C::kBarDqFull), 1);
         mbar_init(BAR(C::kBarDqRead), 256);
@@ -415,10 +414,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
             }
             tc_fence_after();
-            // Per query tile j, in issue order: dP(j); then, once P and dS are
-            // ready, dV(j) (frees dO's buffer), dQ_part(j) (read out while the
-            // rest runs), dK(j) (frees Q's stage and the P, dS buffers), and
-            // S(j+1) into the S columns the elementwise warps have finished with.
+            // Per query tile j, in issue order: dP(j); S(j+1) once the
+            // elementwise warps have read S(j) and dP(j) out of TMEM; then, once
+            // P and dS are ready, dV(j) (frees dO's buffer), dQ_part(j) (read out
+            // while the rest runs) and dK(j) (frees Q's stage and the P, dS
+            // buffers).
             auto issue_s = [&](uint32_t qb) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -445,6 +445,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                               make_sdesc(sV + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(BAR(C::kBarSFull));
+                // S(j+1) as soon as the elementwise warps hold S(j) and dP(j) in registers
+                if (j + 1 < nQ) {
+                    const int sq1 = (j + 1) % NQ;
+                    if (!(ok = wait_b(BAR(C::kBarSRead), j & 1, abort_flag))) break;
+                    if (!(ok = wait_b(BAR(C::kBarQFull + sq1), ((j + 1) / NQ) & 1, abort_flag))) break;
+                    tc_fence_after();
+                    issue_s(sQ + sq1 * C::kTileBytes);
+                }
                 if (!(ok = wait_b(BAR(C::kBarPReady), j & 1, abort_flag))) break;
                 tc_fence_after();
                 // dV += P^T dO and dK += dS^T Q: A = P^T / dS^T, MN-major (keys
@@ -472,12 +480,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                               (j > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(BAR(C::kBarQEmpty + sq));
                 tc_commit(BAR(C::kBarPFree));
-                if (j + 1 < nQ) {
-                    const int sq1 = (j + 1) % NQ;
-                    if (!(ok = wait_b(BAR(C::kBarQFull + sq1), ((j + 1) / NQ) & 1, abort_flag))) break;
-                    tc_fence_after();
-                    issue_s(sQ + sq1 * C::kTileBytes);
-                }
             }
             // every MMA this thread issued completes before the block exits
             tc_commit(BAR(C::kBarDrain));
@@ -581,6 +583,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int c0 = cb + 16 * kk;
                 wait_ld17(a, an[0]);
                 wait_ld17(g, gn[0]);
+                if (kk == 3) {  // every TMEM load of S and dP of this tile has landed
+                    tc_fence_before();
+                    mbar_arrive(BAR(C::kBarSRead));
+                }
                 float sv[17], gv[17];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
