@@ -130,8 +130,10 @@ struct BwCfg {
     static constexpr int kBarDqFull = kBarPReady + 1;       // dV, dQ_part MMAs done
     static constexpr int kBarDqRead = kBarDqFull + 1;       // dQ_part read out of TMEM
     static constexpr int kBarPFree = kBarDqRead + 1;       // dK done: P, dS no longer read
-    static constexpr int kBarStageFull = kBarPFree + 1;    // dQ_part staged (fp32) in P, dS
-    static constexpr int kBarStageFree = kBarStageFull + 1; // its reduction has read it
+    // dQ_part staged (fp32): half 0's columns where P was, half 1's after them
+    // (where dS was, at d = 128)
+    static constexpr int kBarStageFull = kBarPFree + 1;     // [2], one per column half
+    static constexpr int kBarStageFree = kBarStageFull + 2; // its reductions have read it
     static constexpr int kBarDrain = kBarStageFree + 1;
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -329,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(BAR(C::kBarDqFull), 1);
         mbar_init(BAR(C::kBarDqRead), 256);
         mbar_init(BAR(C::kBarPFree), 1);
-        mbar_init(BAR(C::kBarStageFull), 256);
+        mbar_init(BAR(C::kBarStageFull), 128);
+        mbar_init(BAR(C::kBarStageFull + 1), 128);
         mbar_init(BAR(C::kBarStageFree), 1);
         mbar_init(BAR(C::kBarDrain), 1);
         *abort_flag = 0;
@@ -492,13 +495,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // with TMA reductions and frees the staging area once they have read it.
         if (lane == 0) {
             tma_prefetch_desc(&tm_dq);
-            for (int j = 0; j < nQ; ++j) {
-                if (!wait_b(BAR(C::kBarStageFull), j & 1, abort_flag)) break;
+            bool ok = true;
+            for (int j = 0; ok && j < nQ; ++j) {
                 const int row0 = 128 * (q_first + j);
+                // each column half's boxes as soon as that half has staged them
 #pragma unroll
-                for (int b = 0; b < D / 32; ++b)
-                    tma_reduce_add_3d(sP + b * kChunkBytes, &tm_dq, 32 * b, row0, bh);
-                bulk_commit();
+                for (int h = 0; h < 2; ++h) {
+                    if (!(ok = wait_b(BAR(C::kBarStageFull + h), j & 1, abort_flag))) break;
+#pragma unroll
+                    for (int b = h * (D / 64); b < (h + 1) * (D / 64); ++b)
+                        tma_reduce_add_3d(sP + b * kChunkBytes, &tm_dq, 32 * b, row0, bh);
+                    bulk_commit();
+                }
+                if (!ok) break;
                 bulk_wait_read_all();
                 mbar_arrive(BAR(C::kBarStageFree));
             }
@@ -512,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + C::kColS, tD = tmem + lane_off + C::kColP;
         const float k2 = p.k2, scale = p.scale;
+        const bool stage_in_ds = half * (D / 64) >= 2;  // this half's dQ boxes lie where dS was
         bool ok = true;
         // the row statistics of the first query tile; later ones are fetched
         // one tile ahead
@@ -637,10 +647,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int cc = 0; cc < D / 64; ++cc) tmem_wait_ld_regs<32>(o[cc]);
             tc_fence_before();
             mbar_arrive(BAR(C::kBarDqRead));
-            // the staging area is free once dK, the last MMA reading P and dS, is done
-            ok = __all_sync(0xffffffffu, wait_b(BAR(C::kBarPFree), j & 1, abort_flag));
-            if (!ok) break;
-            tc_fence_after();
+            // Boxes where P was are free once dV is done (DqFull covers it);
+            // those where dS was (half 1 at d = 128) once dK, the last MMA
+            // reading dS, is done.
+            if (stage_in_ds) {
+                ok = __all_sync(0xffffffffu, wait_b(BAR(C::kBarPFree), j & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+            }
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 uint8_t *srow = smem + C::kOffP + (half * (D / 64) + cc) * kChunkBytes + irow * 128;
@@ -650,7 +664,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         make_uint4(o[cc][4 * c], o[cc][4 * c + 1], o[cc][4 * c + 2], o[cc][4 * c + 3]);
             }
             fence_proxy_async_smem();
-            mbar_arrive(BAR(C::kBarStageFull));
+            mbar_arrive(BAR(C::kBarStageFull + half));
+        }
+        // the dK of the walk's last tile is complete before it is read out
+        if (ok && !stage_in_ds) {
+            ok = __all_sync(0xffffffffu, wait_b(BAR(C::kBarPFree), (nQ - 1) & 1, abort_flag));
+            tc_fence_after();
         }
         if (ok) {
             // dV, dK of this tile's keys: TMEM lane = key row of the tile.
