@@ -21,7 +21,7 @@ import torch
 import oracle
 from continuous_softmax_attention_gb300 import (CsaError, backward, backward_workspace_bytes,
                                                 forward)
-from continuous_softmax_attention_gb300.inputs import make_inputs
+from continuous_softmax_attention_gb300.inputs import make_inputs, workload_inputs
 from gpu_util import np64
 
 pytestmark = pytest.mark.gpu
@@ -166,3 +166,22 @@ def test_backward_long_rows(T, d, mode):
     x = make_inputs(1, 2, T, d, "bf16", seed=190 + T)
     g = upstream((1, 2, T, d), 13)
     compare(x, g, 1.0 / d ** 0.5, mode, "bf16", f"long T={T} d={d}")
+
+
+def test_backward_headline_shape():
+    """The backward pass at the benchmark's shape (B=1, H=32, T=8192, d=128,
+    zero sink, the same seeded upstream gradient), all heads in one call as
+    the benchmark launches it: two scheduling groups of 16 heads, 65 key
+    tiles per head.  The oracle checks the last head whole (8192 rows of dq,
+    dk, dv; about 40 s of double-precision CPU work)."""
+    x = workload_inputs("headline")
+    B, H, T, d = x["q"].shape
+    scale = 1.0 / d ** 0.5
+    g = torch.randn(B, H, T, d, generator=torch.Generator().manual_seed(7))
+    (dq, dk, dv, _, _), gq = run(x, g, scale, oracle.ZERO)
+    h = H - 1
+    sl = lambda t: t[:, h:h + 1].contiguous()
+    ref = oracle.backward(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(gq).float(), scale=scale,
+                          mode=oracle.ZERO)
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        check(sl(got), ref[name], "bf16", f"headline head {h} {name}")
