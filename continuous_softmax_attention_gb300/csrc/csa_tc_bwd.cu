@@ -621,6 +621,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     cols16<false>(sv, gv, k2, lse2, Dr, scale, c0, c_last, zero_c0, last_chunk,
                                   Lc, Fc, pP, pS);
+                // P and dS overwrite the previous tile's staged dQ_part: wait until
+                // its reductions have read it (the MMAs reading the previous P
+                // and dS finished before this tile's S and dP did)
                 if (kk == 0 && j > 0 &&
                     !__all_sync(0xffffffffu, wait_b(BAR(C::kBarStageFree), (j - 1) & 1, abort_flag))) {
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");  // chunk 1's loads
@@ -634,9 +637,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(BAR(C::kBarPReady));
             // dQ_part of this query tile (in the dP columns): out of TMEM, which
-            // frees the dP columns, then staged in fp32 where P and dS were (the
-            // MMAs that read them are complete), 128B-swizzled boxes of
-            // [128 rows][32 columns] for the reducer warp's TMA reductions
+            // frees the dP columns, then staged in fp32 where P and dS were, as
+            // 128B-swizzled boxes of [128 rows][32 columns] for the reducer
+            // warp's TMA reductions
             ok = __all_sync(0xffffffffu, wait_b(BAR(C::kBarDqFull), j & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
