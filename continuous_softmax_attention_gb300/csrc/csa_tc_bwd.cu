@@ -106,6 +106,23 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 // every committed reduction has completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// A shared-memory descriptor with its low word (start address in 16-byte
+// units, leading byte offset) kept apart, so that each constant offset of an
+// unrolled loop costs one add: an operand inside the 227 KB of shared memory
+// keeps its start address below 2^14 units, so the add never carries out of
+// the field.  The single MMA-issuing thread shares its scheduler with two
+// busy elementwise warps; every instruction it saves shortens its issue.
+struct SDesc {
+    uint32_t lo, hi;
+    __device__ __forceinline__ uint64_t at(uint32_t off_bytes) const {
+        return ((uint64_t)hi << 32) | (uint64_t)(lo + (off_bytes >> 4));
+    }
+};
+__device__ __forceinline__ SDesc sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    const uint64_t d = make_sdesc(saddr, lbo, sbo);
+    return {(uint32_t)d, (uint32_t)(d >> 32)};
+}
+
 template <int D>
 struct BwCfg {
     static constexpr int kChunks = D / 64;
@@ -422,12 +439,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // P and dS are ready, dV(j) (frees dO's buffer), dQ_part(j) (read out
             // while the rest runs) and dK(j) (frees Q's stage and the P, dS
             // buffers).
+            // the fixed operands' descriptors (K-major: LBO 16; MN-major: LBO
+            // one 64-column box)
+            const SDesc dK = sdesc(sK, 16, 1024), dV = sdesc(sV, 16, 1024);
+            const SDesc dKmn = sdesc(sK, kChunkBytes, 1024);
+            const SDesc dPmn = sdesc(sP, kChunkBytes, 1024), dSmn = sdesc(sS, kChunkBytes, 1024);
+            const SDesc dS = sdesc(sS, 16, 1024);
             auto issue_s = [&](uint32_t qb) {
+                const SDesc dQ = sdesc(qb, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    tc_mma_ss(tmem + C::kColS, make_sdesc(qb + off, 16, 1024),
-                              make_sdesc(sK + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                    tc_mma_ss(tmem + C::kColS, dQ.at(off), dK.at(off), kIdS, kk > 0 ? 1u : 0u);
                 }
             };
             if (ok && (ok = wait_b(BAR(C::kBarQFull), 0, abort_flag))) {
@@ -441,11 +464,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j > 0 && !(ok = wait_b(BAR(C::kBarDqRead), (j - 1) & 1, abort_flag))) break;
                 if (!(ok = wait_b(BAR(C::kBarGFull + sg), (j / NG) & 1, abort_flag))) break;
                 tc_fence_after();
+                const SDesc dG = sdesc(gb, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    tc_mma_ss(tmem + C::kColP, make_sdesc(gb + off, 16, 1024),
-                              make_sdesc(sV + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                    tc_mma_ss(tmem + C::kColP, dG.at(off), dV.at(off), kIdS, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(BAR(C::kBarSFull));
                 // S(j+1) as soon as the elementwise warps hold S(j) and dP(j) in registers
@@ -461,10 +484,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // dV += P^T dO and dK += dS^T Q: A = P^T / dS^T, MN-major (keys
                 // contiguous, two 64-key boxes); B = dO / Q, MN-major; the
                 // reduction runs over the 128 query rows, 16 per step.
+                const SDesc dGmn = sdesc(gb, kChunkBytes, 1024), dQmn = sdesc(qb, kChunkBytes, 1024);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_ss(tmem + C::kColV, make_sdesc(sP + kk * 2048, kChunkBytes, 1024),
-                              make_sdesc(gb + kk * 2048, kChunkBytes, 1024), kIdKV,
+                    tc_mma_ss(tmem + C::kColV, dPmn.at(kk * 2048), dGmn.at(kk * 2048), kIdKV,
                               (j > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(BAR(C::kBarGEmpty + sg));
                 // dQ_part = dS K: A = dS K-major (reduction over the 128 keys),
@@ -472,14 +495,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    tc_mma_ss(tmem + C::kColP, make_sdesc(sS + off, 16, 1024),
-                              make_sdesc(sK + kk * 2048, kChunkBytes, 1024), kIdQ, kk > 0 ? 1u : 0u);
+                    tc_mma_ss(tmem + C::kColP, dS.at(off), dKmn.at(kk * 2048), kIdQ, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(BAR(C::kBarDqFull));
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_ss(tmem + C::kColK, make_sdesc(sS + kk * 2048, kChunkBytes, 1024),
-                              make_sdesc(qb + kk * 2048, kChunkBytes, 1024), kIdKV,
+                    tc_mma_ss(tmem + C::kColK, dSmn.at(kk * 2048), dQmn.at(kk * 2048), kIdKV,
                               (j > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(BAR(C::kBarQEmpty + sq));
                 tc_commit(BAR(C::kBarPFree));
