@@ -11,7 +11,10 @@ from ._lib import (  # noqa: F401
     backward,
     backward_workspace_bytes,
     decode,
+    decode_merge_ranges,
     decode_noalloc,
+    decode_range,
+    decode_range_workspace_bytes,
     decode_workspace_bytes,
     device_status,
     forward,
@@ -21,6 +24,7 @@ from ._lib import (  # noqa: F401
     logphi2_eval,
     segment_weights_eval,
     selftest_wait_timeout,
+    shard_rows,
     status_string,
     std_forward,
 )
@@ -29,6 +33,8 @@ __all__ = [
     "ZERO", "COPY_FIRST", "GIVEN", "CsaError", "forward", "forward_host",
     "forward_host_workspace_bytes", "forward_symmetric", "std_forward",
     "backward",
-    "backward_workspace_bytes", "decode", "decode_noalloc", "decode_workspace_bytes", "logphi2_eval",
+    "backward_workspace_bytes", "decode", "decode_noalloc", "decode_workspace_bytes",
+    "decode_range", "decode_range_workspace_bytes", "decode_merge_ranges", "shard_rows",
+    "logphi2_eval",
     "segment_weights_eval", "device_status", "selftest_wait_timeout", "status_string",
 ]

@@ -60,6 +60,9 @@ def load():
                        ("csa_decode", [p, p, p, p, p, p, p, p, p, ctypes.c_longlong, i, i, i, i,
                                        f, i, p]),
                        ("csa_decode_noalloc", [p, p, p, p, p, p, p, p, i, i, i, i, f, i, p]),
+                       ("csa_decode_range", [p, p, p, p, p, p, p, p, p, ctypes.c_longlong, i, i,
+                                             i, i, f, i, i, i, p]),
+                       ("csa_decode_merge_ranges", [p, p, i, i, i, i, p, p, p]),
                        ("csa_backward", bwd), ("csa_backward_f32", bwd),
                        ("csa_forward_host", [p, p, p, p, p, p, p, p, ctypes.c_longlong, i, i, i,
                                              i, f, i, i, p, p, p])):
@@ -70,6 +73,8 @@ def load():
                  "csa_forward_host_workspace_bytes"):
         getattr(lib, name).argtypes = [i, i, i, i]
         getattr(lib, name).restype = ctypes.c_longlong
+    lib.csa_decode_range_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.csa_decode_range_workspace_bytes.restype = ctypes.c_longlong
     lib.csa_status_string.argtypes = [i]
     lib.csa_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -298,6 +303,92 @@ def decode(q, k_cache, v_cache, k0=None, v0=None, *, seqlens=None, mode: int = 0
     _check(load().csa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k0), _ptr(v0),
                              _ptr(seqlens), _ptr(out), _ptr(lse), _ptr(workspace), nbytes, B, H,
                              T, d, float(scale), int(mode), _stream_handle(stream)), "csa_decode")
+    return out, lse
+
+
+def decode_range_workspace_bytes(B: int, H: int, pos_lo: int, pos_hi: int, d: int) -> int:
+    """Bytes of workspace csa_decode_range needs (host-side, no device needed)."""
+    n = int(load().csa_decode_range_workspace_bytes(int(B), int(H), int(pos_lo), int(pos_hi),
+                                                    int(d)))
+    if n < 0:
+        raise CsaError(CSA_ERR_UNSUPPORTED, "csa_decode_range_workspace_bytes")
+    return n
+
+
+def shard_rows(T: int, pos_lo: int, pos_hi: int):
+    """Cache rows [start, stop) a range's shard holds: its positions and one
+    neighbour on each side (position i >= 1 is cache row i - 1)."""
+    return max(pos_lo - 2, 0), min(pos_hi, T)
+
+
+def decode_range(q, k_shard, v_shard, T: int, pos_lo: int, pos_hi: int, k0=None, v0=None, *,
+                 seqlens=None, mode: int = 0, scale=None, out=None, lse=None, workspace=None,
+                 stream=None):
+    """The decode step over the positions [pos_lo, pos_hi) of each row only
+    (csa_decode_range): one range of a cache split along its time axis.
+
+    q: bf16 CUDA [B, H, d]; k_shard, v_shard: bf16 [B, H, rows, d] holding the
+    cache rows shard_rows(T, pos_lo, pos_hi); T: the whole cache's capacity.
+    Returns (o_r fp32 [B, H, d], lse_r fp32 [B, H]) for decode_merge_ranges."""
+    import torch
+
+    B, H, rows, d = k_shard.shape
+    dev = k_shard.device
+    bf = torch.bfloat16
+    r0, r1 = shard_rows(T, pos_lo, pos_hi)
+    if rows != r1 - r0:
+        raise ValueError(f"the shard of positions [{pos_lo}, {pos_hi}) holds {r1 - r0} rows")
+    _check_tensor(k_shard, "k_shard", bf, (B, H, rows, d), dev)
+    _check_tensor(v_shard, "v_shard", bf, (B, H, rows, d), dev)
+    _check_tensor(q, "q", bf, (B, H, d), dev)
+    if mode == 2:
+        if k0 is None or v0 is None:
+            raise ValueError("mode 2 (given sink) needs k0 and v0")
+        _check_tensor(k0, "k0", bf, (H, d), dev)
+        _check_tensor(v0, "v0", bf, (H, d), dev)
+    else:
+        k0 = v0 = None
+    if seqlens is not None:
+        _check_tensor(seqlens, "seqlens", torch.int32, (B,), dev)
+    if scale is None:
+        scale = 1.0 / d ** 0.5
+    if out is None:
+        out = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    _check_tensor(out, "out", torch.float32, (B, H, d), dev)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    _check_tensor(lse, "lse", torch.float32, (B, H), dev)
+    if workspace is None:
+        workspace = torch.empty(max(decode_range_workspace_bytes(B, H, pos_lo, pos_hi, d), 16),
+                                dtype=torch.uint8, device=dev)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().csa_decode_range(_ptr(q), _ptr(k_shard), _ptr(v_shard), _ptr(k0), _ptr(v0),
+                                   _ptr(seqlens), _ptr(out), _ptr(lse), _ptr(workspace), nbytes,
+                                   B, H, int(T), d, float(scale), int(mode), int(pos_lo),
+                                   int(pos_hi), _stream_handle(stream)), "csa_decode_range")
+    return out, lse
+
+
+def decode_merge_ranges(o_parts, lse_parts, *, out=None, lse=None, stream=None):
+    """lse-weighted merge of range partials (csa_decode_merge_ranges).
+
+    o_parts: fp32 CUDA [R, B, H, d]; lse_parts: fp32 [R, B, H].
+    Returns (o bf16 [B, H, d], lse fp32 [B, H])."""
+    import torch
+
+    R, B, H, d = o_parts.shape
+    dev = o_parts.device
+    _check_tensor(o_parts, "o_parts", torch.float32, (R, B, H, d), dev)
+    _check_tensor(lse_parts, "lse_parts", torch.float32, (R, B, H), dev)
+    if out is None:
+        out = torch.empty((B, H, d), dtype=torch.bfloat16, device=dev)
+    _check_tensor(out, "out", torch.bfloat16, (B, H, d), dev)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    _check_tensor(lse, "lse", torch.float32, (B, H), dev)
+    _check(load().csa_decode_merge_ranges(_ptr(o_parts), _ptr(lse_parts), R, B, H, d, _ptr(out),
+                                          _ptr(lse), _stream_handle(stream)),
+           "csa_decode_merge_ranges")
     return out, lse
 
 

@@ -114,6 +114,36 @@ int decode_bf16(const void *q, const void *k_cache, const void *v_cache, const v
                           scale, mode, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int decode_range_bf16(const void *q, const void *k_shard, const void *v_shard, const void *k0,
+                      const void *v0, const int *seqlens, float *out, float *lse,
+                      void *workspace, long long workspace_bytes, int B, int H, int T, int d,
+                      float scale, int mode, int pos_lo, int pos_hi, csa_stream_t stream) {
+    if (B < 0 || H < 0 || T < 0 || d < 1) return CSA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return CSA_ERR_INVALID_ARG;
+    if (mode < CSA_K0_ZERO || mode > CSA_K0_GIVEN) return CSA_ERR_INVALID_ARG;
+    if (!(d == 64 || d == 128 || d == 256)) return CSA_ERR_UNSUPPORTED;
+    // positions 0..T exist; a range may not start right after the sink
+    if (pos_lo < 0 || pos_lo == 1 || pos_hi <= pos_lo || (long long)pos_hi > (long long)T + 1)
+        return CSA_ERR_INVALID_ARG;
+    if ((long long)B * H == 0) return CSA_OK;
+    if (T == 0) return CSA_ERR_INVALID_ARG;
+    if (!q || !k_shard || !v_shard || !out || !lse || !workspace) return CSA_ERR_INVALID_ARG;
+    if (mode == CSA_K0_GIVEN && (!k0 || !v0)) return CSA_ERR_INVALID_ARG;
+    if ((long long)B * H * T > (1LL << 40)) return CSA_ERR_UNSUPPORTED;
+    const long long need = csa_decode_range_scratch_bytes(B, H, pos_lo, pos_hi, d);
+    if (need < 0) return CSA_ERR_UNSUPPORTED;
+    if (workspace_bytes < need) return CSA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_shard, 16) || !aligned(v_shard, 16) || !aligned(out, 16) ||
+        !aligned(workspace, 16) || !aligned(lse, 4) || (seqlens && !aligned(seqlens, 4)))
+        return CSA_ERR_ALIGNMENT;
+    if (mode == CSA_K0_GIVEN && (!aligned(k0, 16) || !aligned(v0, 16))) return CSA_ERR_ALIGNMENT;
+    int rc = device_ok();
+    if (rc != CSA_OK) return rc;
+    return csa_decode_range_run(q, k_shard, v_shard, k0, v0, seqlens, out, lse, workspace, B, H, T,
+                                d, scale, mode, pos_lo, pos_hi,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
 long long backward_scratch_bytes(int B, int H, int T, int d) {
     if (B < 0 || H < 0 || T < 0 || d < 1 || d > 256) return -1;
     const long long a = csa_simt_backward_scratch_bytes(B, H, T, d);
@@ -225,6 +255,32 @@ int csa_forward_host(const void *q, const void *k, const void *v, const void *k0
                             heads_per_chunk, reinterpret_cast<cudaStream_t>(stream),
                             reinterpret_cast<cudaStream_t>(stream_h2d),
                             reinterpret_cast<cudaStream_t>(stream_d2h));
+}
+
+long long csa_decode_range_workspace_bytes(int B, int H, int pos_lo, int pos_hi, int d) {
+    return csa_decode_range_scratch_bytes(B, H, pos_lo, pos_hi, d);
+}
+
+int csa_decode_range(const void *q, const void *k_shard, const void *v_shard, const void *k0,
+                     const void *v0, const int *seqlens, float *out, float *lse, void *workspace,
+                     long long workspace_bytes, int B, int H, int T, int d, float scale,
+                     int k0_mode, int pos_lo, int pos_hi, csa_stream_t stream) {
+    return decode_range_bf16(q, k_shard, v_shard, k0, v0, seqlens, out, lse, workspace,
+                             workspace_bytes, B, H, T, d, scale, k0_mode, pos_lo, pos_hi, stream);
+}
+
+int csa_decode_merge_ranges(const float *o_parts, const float *lse_parts, int R, int B, int H,
+                            int d, void *out, float *lse, csa_stream_t stream) {
+    if (R < 1 || B < 0 || H < 0 || d < 1 || d > 256) return CSA_ERR_INVALID_ARG;
+    if ((long long)B * H == 0) return CSA_OK;
+    if (!o_parts || !lse_parts || !out) return CSA_ERR_INVALID_ARG;
+    if ((long long)R * B * H * d > (1LL << 40)) return CSA_ERR_UNSUPPORTED;
+    if (!aligned(o_parts, 4) || !aligned(lse_parts, 4) || !aligned(out, 2) || (lse && !aligned(lse, 4)))
+        return CSA_ERR_ALIGNMENT;
+    int rc = device_ok();
+    if (rc != CSA_OK) return rc;
+    return csa_decode_merge_ranges_run(o_parts, lse_parts, R, B, H, d, out, lse,
+                                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 long long csa_decode_workspace_bytes(int B, int H, int T, int d) {

@@ -78,9 +78,13 @@ struct DecParams {
     const int *seqlens;
     float *part_o;   // [B*H][S][D]: unnormalised partial outputs
     float *part_ml;  // [B*H][S][2]: chunk maximum (log2 units), chunk weight sum
-    __nv_bfloat16 *out;
+    __nv_bfloat16 *out;  // o in bf16, or
+    float *out_f32;      // o in fp32 (a range's partial output)
     float *lse;
     int B, H, T, S;
+    int rows;      // cache rows per (b, h) in k, v: T, or a shard's rows
+    int row_base;  // cache row held in row 0 of k, v
+    int pos_lo, pos_hi;  // owned positions [pos_lo, pos_hi): 0, T + 1 for a whole row
     float qscale;  // scale * log2(e): logits come out in log2 units
     int mode;
 };
@@ -185,13 +189,14 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(const DecParams 
     const int bh = blockIdx.x / p.S, chunk = blockIdx.x - bh * p.S;
     const int b = bh / p.H, h = bh - b * p.H;
     const int n = p.seqlens ? p.seqlens[b] : p.T;
-    const int P0 = chunk * C;
+    const int P0 = p.pos_lo + chunk * C;
     if (n < 1 || n > p.T || P0 > n) return;  // no position of this chunk exists
-    const int P1 = min(P0 + C, n + 1);        // owned positions [P0, P1)
+    const int P1 = min(min(P0 + C, p.pos_hi), n + 1);  // owned positions [P0, P1)
     const int own = P1 - P0;
     const int kp_lo = max(P0 - 1, 1), kp_hi = min(P1, n);  // cached keys staged
     const int vp_lo = max(P0, 1);                          // cached values staged: [vp_lo, P1)
-    const size_t head = (size_t)bh * p.T;
+    // position pos >= 1 is cache row pos - 1, held in row pos - 1 - row_base
+    const long long head = (long long)bh * p.rows - p.row_base;
     // Shared-memory slot of position pos: keys pos - P0 + 1, values pos - P0.
 
     if (tid == 0) {
@@ -358,16 +363,27 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecPa
     __shared__ float part[kParts][D];
     const int bh = blockIdx.x, b = bh / p.H, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = p.seqlens ? p.seqlens[b] : p.T;
-    __nv_bfloat16 *out = p.out + (size_t)bh * D;
+    auto store = [&](int col, float val) {
+        if (p.out_f32)
+            p.out_f32[(size_t)bh * D + col] = val;
+        else
+            p.out[(size_t)bh * D + col] = __float2bfloat16_rn(val);
+    };
     if (n < 1 || n > p.T) {  // a length outside [1, T]: NaN result, status word set
-        for (int col = tid; col < D; col += kMergeThreads) out[col] = __float2bfloat16_rn(NAN);
+        for (int col = tid; col < D; col += kMergeThreads) store(col, NAN);
         if (tid == 0) {
             if (p.lse) p.lse[bh] = NAN;
             atomicCAS(&g_dec_status, 0, CSA_ERR_INVALID_ARG);
         }
         return;
     }
-    const int nch = n / C + 1;  // chunks holding positions 0..n
+    if (p.pos_lo > n) {  // a range past this sequence's end: an empty partial
+        for (int col = tid; col < D; col += kMergeThreads) store(col, 0.0f);
+        if (tid == 0 && p.lse) p.lse[bh] = -INFINITY;
+        return;
+    }
+    // chunks holding the owned positions [pos_lo, min(pos_hi, n + 1))
+    const int nch = (min(p.pos_hi, n + 1) - p.pos_lo + C - 1) / C;
     const float *ml = p.part_ml + (size_t)bh * p.S * 2;
     const float *po = p.part_o + (size_t)bh * p.S * D;
     float M = -INFINITY;
@@ -404,15 +420,43 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecPa
         float s = acc;
 #pragma unroll
         for (int i = 1; i < kParts; ++i) s += part[i][col];
-        out[col] = __float2bfloat16_rn(s * (1.0f / L));
+        store(col, s * (1.0f / L));
     }
     if (tid == 0 && p.lse) p.lse[bh] = (M + log2f(L)) * kLn2;
+}
+
+// Merge of R partial results of the same rows, one per range of positions
+// (eq. (11) restricted to the range's keys): with L the largest lse_r,
+//     o = sum_r e^{lse_r - L} o_r / sum_r e^{lse_r - L},
+//     lse = L + log sum_r e^{lse_r - L};
+// an empty range (lse_r = -inf) weighs nothing.  One warp per row.
+__global__ void __launch_bounds__(256) merge_ranges_kernel(const float *o_parts,
+                                                           const float *lse_parts, int R,
+                                                           long long rows, int d,
+                                                           __nv_bfloat16 *out, float *lse) {
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    float L = -INFINITY;
+    for (int r = 0; r < R; ++r) L = fmaxf(L, lse_parts[(long long)r * rows + row]);
+    float den = 0.0f;
+    for (int r = 0; r < R; ++r) den += ex2_approx((lse_parts[(long long)r * rows + row] - L) * kLog2e);
+    const float inv = 1.0f / den;
+    for (int col = lane; col < d; col += 32) {
+        float num = 0.0f;
+        for (int r = 0; r < R; ++r) {
+            const float w = ex2_approx((lse_parts[(long long)r * rows + row] - L) * kLog2e);
+            num = fmaf(w, o_parts[((long long)r * rows + row) * d + col], num);
+        }
+        out[row * d + col] = __float2bfloat16_rn(num * inv);
+    }
+    if (lane == 0 && lse) lse[row] = L + logf(den);
 }
 
 template <int D>
 int launch_decode(DecParams p, cudaStream_t stream) {
     using Cf = DecCfg<D>;
-    p.S = p.T / Cf::C + 1;
+    p.S = (p.pos_hi - p.pos_lo + Cf::C - 1) / Cf::C;  // chunks of the owned positions
     const long long BH = (long long)p.B * p.H;
     const long long grid = BH * p.S;
     if (grid > 0x7fffffffLL || BH > 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
@@ -430,36 +474,80 @@ int chunk_positions(int d) { return d == 64 ? DecCfg<64>::C : d == 128 ? DecCfg<
 }  // namespace
 
 long long csa_decode_scratch_bytes(int B, int H, int T, int d) {
-    if (B < 0 || H < 0 || T < 0 || !(d == 64 || d == 128 || d == 256)) return -1;
-    const long long S = (long long)T / chunk_positions(d) + 1;
+    return csa_decode_range_scratch_bytes(B, H, 0, T + 1, d);
+}
+
+long long csa_decode_range_scratch_bytes(int B, int H, int pos_lo, int pos_hi, int d) {
+    if (B < 0 || H < 0 || pos_lo < 0 || pos_hi < pos_lo || !(d == 64 || d == 128 || d == 256))
+        return -1;
+    const int C = chunk_positions(d);
+    const long long S = ((long long)pos_hi - pos_lo + C - 1) / C;
     return (long long)B * H * S * (d + 2) * (long long)sizeof(float);
 }
 
-int csa_decode_run(const void *q, const void *k_cache, const void *v_cache, const void *k0,
-                   const void *v0, const int *seqlens, void *out, float *lse, void *scratch, int B,
-                   int H, int T, int d, float scale, int mode, cudaStream_t stream) {
+namespace {
+
+int run_range(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+              const int *seqlens, void *out, float *out_f32, float *lse, void *scratch, int B,
+              int H, int T, int d, float scale, int mode, int pos_lo, int pos_hi,
+              cudaStream_t stream) {
     DecParams p;
     p.q = static_cast<const __nv_bfloat16 *>(q);
-    p.k = static_cast<const __nv_bfloat16 *>(k_cache);
-    p.v = static_cast<const __nv_bfloat16 *>(v_cache);
+    p.k = static_cast<const __nv_bfloat16 *>(k);
+    p.v = static_cast<const __nv_bfloat16 *>(v);
     p.k0 = static_cast<const __nv_bfloat16 *>(k0);
     p.v0 = static_cast<const __nv_bfloat16 *>(v0);
     p.seqlens = seqlens;
-    const long long S = (long long)T / chunk_positions(d) + 1;
+    const int C = chunk_positions(d);
+    const long long S = ((long long)pos_hi - pos_lo + C - 1) / C;
     p.part_o = static_cast<float *>(scratch);
     p.part_ml = p.part_o + (long long)B * H * S * d;
     p.out = static_cast<__nv_bfloat16 *>(out);
+    p.out_f32 = out_f32;
     p.lse = lse;
     p.B = B;
     p.H = H;
     p.T = T;
     p.S = (int)S;
+    // a range's shard holds cache rows [max(pos_lo - 2, 0), min(pos_hi, T)): its
+    // positions and the neighbour on each side
+    p.row_base = pos_lo >= 2 ? pos_lo - 2 : 0;
+    p.rows = min(pos_hi, T) - p.row_base;
+    p.pos_lo = pos_lo;
+    p.pos_hi = pos_hi;
     p.qscale = scale * kLog2e;
     p.mode = mode;
     if (d == 128) return launch_decode<128>(p, stream);
     if (d == 64) return launch_decode<64>(p, stream);
     if (d == 256) return launch_decode<256>(p, stream);
     return CSA_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+int csa_decode_run(const void *q, const void *k_cache, const void *v_cache, const void *k0,
+                   const void *v0, const int *seqlens, void *out, float *lse, void *scratch, int B,
+                   int H, int T, int d, float scale, int mode, cudaStream_t stream) {
+    return run_range(q, k_cache, v_cache, k0, v0, seqlens, out, nullptr, lse, scratch, B, H, T, d,
+                     scale, mode, 0, T + 1, stream);
+}
+
+int csa_decode_merge_ranges_run(const float *o_parts, const float *lse_parts, int R, int B, int H,
+                                int d, void *out, float *lse, cudaStream_t stream) {
+    const long long rows = (long long)B * H;
+    const long long blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
+    merge_ranges_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        o_parts, lse_parts, R, rows, d, static_cast<__nv_bfloat16 *>(out), lse);
+    return cudaGetLastError() == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+}
+
+int csa_decode_range_run(const void *q, const void *k_shard, const void *v_shard, const void *k0,
+                         const void *v0, const int *seqlens, float *out, float *lse,
+                         void *scratch, int B, int H, int T, int d, float scale, int mode,
+                         int pos_lo, int pos_hi, cudaStream_t stream) {
+    return run_range(q, k_shard, v_shard, k0, v0, seqlens, nullptr, out, lse, scratch, B, H, T, d,
+                     scale, mode, pos_lo, pos_hi, stream);
 }
 
 // Scratch of csa_decode_noalloc: a file-scope device array, so that the

@@ -42,6 +42,17 @@ long long csa_decode_scratch_bytes(int B, int H, int T, int d);
 int csa_decode_run(const void *q, const void *k_cache, const void *v_cache, const void *k0,
                    const void *v0, const int *seqlens, void *out, float *lse, void *scratch, int B,
                    int H, int T, int d, float scale, int mode, cudaStream_t stream);
+// The same for the owned positions [pos_lo, pos_hi) of each row only, from a
+// cache shard holding rows [max(pos_lo - 2, 0), min(pos_hi, T)); o in fp32.
+long long csa_decode_range_scratch_bytes(int B, int H, int pos_lo, int pos_hi, int d);
+int csa_decode_range_run(const void *q, const void *k_shard, const void *v_shard, const void *k0,
+                         const void *v0, const int *seqlens, float *out, float *lse,
+                         void *scratch, int B, int H, int T, int d, float scale, int mode,
+                         int pos_lo, int pos_hi, cudaStream_t stream);
+// lse-weighted merge of R such partials ([R][B*H][d] and [R][B*H], fp32)
+// into o (bf16) and lse.
+int csa_decode_merge_ranges_run(const float *o_parts, const float *lse_parts, int R, int B, int H,
+                                int d, void *out, float *lse, cudaStream_t stream);
 int csa_decode_take_status(void);
 // Address of the file-scope scratch array of csa_decode_noalloc on the
 // current device (looked up once per device).

@@ -162,3 +162,71 @@ def decode_sharded(q, k_cache, v_cache, k0=None, v0=None, *, seqlens=None, mode:
     o_full = torch.cat([go[r][: b - a] for r, (a, b) in enumerate(sizes)])
     l_full = torch.cat([gl[r][: b - a] for r, (a, b) in enumerate(sizes)])
     return o_full, l_full
+
+
+# ---------------------------------------------------------------- context parallelism
+# One long sequence's KV cache split along its time axis: rank r owns the
+# positions [lo_r, hi_r) of every row (position 0 the sink, position i >= 1
+# cache row i - 1) and holds those cache rows plus one neighbour on each
+# side, which the correction b of its first and last positions needs.  Each
+# rank computes the partial (o_r, lse_r) of its positions; one all-gather and
+# an lse-weighted merge give the whole row's result.  This is the only
+# exchange step of the decode path.
+
+
+def context_ranges(T: int, world: int):
+    """Contiguous, balanced ranges [lo, hi) partitioning the positions 0..T
+    over `world` ranks.  No range starts at position 1 (right after the
+    sink), so a cut that would fall there moves to 2; every range is
+    non-empty, which needs T + 1 >= 2 * world."""
+    if world < 1 or T + 1 < 2 * world:
+        raise ValueError("need T + 1 >= 2 * world positions")
+    cuts = [0]
+    for r in range(1, world):
+        c = (r * (T + 1)) // world
+        cuts.append(max(c, cuts[-1] + 1, 2))
+    cuts.append(T + 1)
+    for a, b in zip(cuts, cuts[1:]):
+        if b <= a:
+            raise ValueError("positions too few for the ranks")
+    return list(zip(cuts[:-1], cuts[1:]))
+
+
+def cache_shard(k_cache, v_cache, pos_lo: int, pos_hi: int):
+    """The cache rows a range's rank holds: [max(pos_lo - 2, 0), min(pos_hi, T))."""
+    T = k_cache.shape[2]
+    r0, r1 = max(pos_lo - 2, 0), min(pos_hi, T)
+    return k_cache[:, :, r0:r1].contiguous(), v_cache[:, :, r0:r1].contiguous()
+
+
+def gather_parts(o_r, lse_r, group=None):
+    """All-gather of every rank's partial: ([R, B, H, d], [R, B, H])."""
+    world = dist.get_world_size(group) if dist.is_initialized() else 1
+    if world == 1:
+        return o_r.unsqueeze(0), lse_r.unsqueeze(0)
+    go = [torch.empty_like(o_r) for _ in range(world)]
+    gl = [torch.empty_like(lse_r) for _ in range(world)]
+    dist.all_gather(go, o_r.contiguous(), group=group)
+    dist.all_gather(gl, lse_r.contiguous(), group=group)
+    return torch.stack(go), torch.stack(gl)
+
+
+def decode_context_parallel(q, k_shard, v_shard, T: int, k0=None, v0=None, *, seqlens=None,
+                            mode: int = 0, scale=None, group=None, fn=None, merge_fn=None):
+    """A decode step with the cache split along time across the ranks of
+    `group` (context_ranges(T, world)[rank] is this rank's range, k_shard and
+    v_shard its cache_shard).  fn computes the partial of this rank's
+    positions (the CUDA csa_decode_range by default), merge_fn merges the
+    gathered partials (csa_decode_merge_ranges by default).  Every rank gets
+    the whole result (o, lse)."""
+    world = dist.get_world_size(group) if dist.is_initialized() else 1
+    rank = dist.get_rank(group) if dist.is_initialized() else 0
+    lo, hi = context_ranges(T, world)[rank]
+    if fn is None:
+        from . import decode_range as fn
+    if merge_fn is None:
+        from . import decode_merge_ranges as merge_fn
+    o_r, lse_r = fn(q, k_shard, v_shard, T, lo, hi, k0, v0, seqlens=seqlens, mode=mode,
+                    scale=scale)
+    o_parts, lse_parts = gather_parts(o_r, lse_r, group)
+    return merge_fn(o_parts, lse_parts)

@@ -309,6 +309,55 @@ int csa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, 
 long long csa_decode_workspace_bytes(int B, int H, int T, int d);
 
 /*
+ * csa_decode_range - the decode step restricted to the positions [pos_lo,
+ *   pos_hi) of every row (position 0 is the sink, position i >= 1 is cache
+ *   row i - 1), for a KV cache whose time axis is split across devices
+ *   (context parallelism).  The pages have no counterpart; it is eq. (11)
+ *   ("Assembly and Simplification" of "Continuous Softmax Attention")
+ *   summed over the owned positions only, each position's weight e^{a+b}
+ *   still taking its correction b from both neighbours (eq. (10)), so that
+ *   merging the ranges of a partition of [0, n] with csa_decode_merge_ranges
+ *   gives csa_decode's result.
+ *   q: DEVICE bf16 [B, H, d]; seqlens, k0, v0, scale, k0_mode, T and d as
+ *   csa_decode (T is the capacity of the whole cache, 1 <= n_b <= T).
+ *   k_shard, v_shard: DEVICE bf16 [B, H, rows, d] holding the cache rows
+ *   [max(pos_lo - 2, 0), min(pos_hi, T)), rows = min(pos_hi, T) -
+ *   max(pos_lo - 2, 0): the owned positions and one neighbour on each side.
+ *   0 <= pos_lo < pos_hi <= T + 1 and pos_lo != 1 (a range cannot start
+ *   right after the sink); otherwise CSA_ERR_INVALID_ARG.
+ *   out: DEVICE fp32 [B, H, d], the range's normalised output o_r;
+ *   lse: DEVICE fp32 [B, H] (required), log of the range's weight sum.  A
+ *   row whose length n_b < pos_lo has no owned position: o_r = 0 and
+ *   lse_r = -inf.
+ *   workspace: DEVICE scratch of csa_decode_range_workspace_bytes(B, H,
+ *   pos_lo, pos_hi, d) bytes, 16-byte aligned.  Tensors 16-byte aligned,
+ *   lse and seqlens 4-byte aligned.  Errors as csa_decode.
+ */
+int csa_decode_range(const void *q, const void *k_shard, const void *v_shard, const void *k0,
+                     const void *v0, const int *seqlens, float *out, float *lse, void *workspace,
+                     long long workspace_bytes, int B, int H, int T, int d, float scale,
+                     int k0_mode, int pos_lo, int pos_hi, csa_stream_t stream);
+
+/* csa_decode_range_workspace_bytes - workspace bytes csa_decode_range needs
+ * (host only), or -1 for a negative size, pos_hi < pos_lo or d outside
+ * {64, 128, 256}. */
+long long csa_decode_range_workspace_bytes(int B, int H, int pos_lo, int pos_hi, int d);
+
+/*
+ * csa_decode_merge_ranges - merges R partial results of the same rows (from
+ *   csa_decode_range over ranges that partition each row's positions):
+ *       o = sum_r e^{lse_r - L} o_r / sum_r e^{lse_r - L},
+ *       lse = L + log sum_r e^{lse_r - L},   L = max_r lse_r;
+ *   an empty range (lse_r = -inf) weighs nothing.  The pages have no
+ *   counterpart: this is the one exchange step of context parallelism.
+ *   o_parts: DEVICE fp32 [R, B, H, d]; lse_parts: DEVICE fp32 [R, B, H];
+ *   out: DEVICE bf16 [B, H, d]; lse: DEVICE fp32 [B, H] or NULL.
+ *   R >= 1, 1 <= d <= 256; CSA_ERR_INVALID_ARG otherwise.
+ */
+int csa_decode_merge_ranges(const float *o_parts, const float *lse_parts, int R, int B, int H,
+                            int d, void *out, float *lse, csa_stream_t stream);
+
+/*
  * csa_logphi2_eval - y[i] = log phi2(x[i]) with the library's fp32 device
  *   function (phi2 of eq. (6), "Preliminaries").  x, y: device float arrays
  *   of n elements (n >= 0).  A test hook for the numerics of b.

@@ -294,6 +294,52 @@ def row_bias(q, k, b, h, r, k0=None, scale=None, mode=ZERO):
     return a, bb
 
 
+def decode_range(q, k_cache, v_cache, seqlens, pos_lo, pos_hi, k0=None, v0=None, scale=None,
+                 mode=ZERO):
+    """The decode step restricted to the positions [pos_lo, pos_hi) of each
+    row (position 0 the sink, position i >= 1 cache row i - 1): eq. (11) of
+    row t = n_b summed over those positions only, each weight e^{a+b} with b
+    from both neighbours (eq. (10), via row_bias).
+
+    q: [B, H, d]; k_cache, v_cache: [B, H, T, d]; seqlens: B lengths.
+    Returns (o [B, H, d], lse [B, H]) in float64; a row with no position in
+    the range gives o = 0 and lse = -inf.  Ranges that partition [0, n_b]
+    merge, weighted by e^{lse}, into the whole row's o and lse."""
+    q = _f32(q)
+    k, v = _f32(k_cache), _f32(v_cache)
+    B, H, T, d = k.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    k0 = _f32(k0) if mode == GIVEN else None
+    v0 = _f32(v0) if mode == GIVEN else None
+    o = np.zeros((B, H, d), dtype=np.float64)
+    lse = np.full((B, H), -np.inf, dtype=np.float64)
+    for b in range(B):
+        n = int(seqlens[b])
+        lo, hi = pos_lo, min(pos_hi, n + 1)
+        if lo >= hi:
+            continue
+        for h in range(H):
+            qrow = np.zeros((1, 1, n, d), dtype=np.float32)
+            qrow[0, 0, n - 1] = q[b, h]
+            kh = np.ascontiguousarray(k[b:b + 1, h:h + 1, :n])
+            a, bb = row_bias(qrow, kh, 0, 0, n - 1, k0[h:h + 1] if k0 is not None else None,
+                             scale=scale, mode=mode)
+            z = (a + bb)[lo:hi]
+            m = z.max()
+            w = np.exp(z - m)
+            if mode == GIVEN:
+                sink_v = v0[h].astype(np.float64)
+            elif mode == COPY_FIRST:
+                sink_v = v[b, h, 0].astype(np.float64)
+            else:
+                sink_v = np.zeros(d)
+            vals = np.vstack([sink_v[None], v[b, h, :n].astype(np.float64)])[lo:hi]
+            o[b, h] = (w[:, None] * vals).sum(axis=0) / w.sum()
+            lse[b, h] = m + np.log(w.sum())
+    return o, lse
+
+
 def log_dphi2(x: float) -> float:
     """log phi2'(x), phi2'(x) = int_0^1 s (1 - s) e^{sx} ds."""
     return _load().csa_oracle_log_dphi2(float(x))

@@ -133,6 +133,52 @@ def test_decode_validation(lib):
         assert dec(lib, ws_bytes=need) == L.CSA_ERR_NO_DEVICE
 
 
+def dec_range(lib, *, q=FAKE, k=FAKE, v=FAKE, k0=NULL, v0=NULL, seqlens=NULL, out=FAKE, lse=FAKE,
+              ws=FAKE, ws_bytes=1 << 30, B=2, H=2, T=300, d=128, scale=0.1, mode=0, lo=0, hi=150):
+    return lib.csa_decode_range(q, k, v, k0, v0, seqlens, out, lse, ws, ws_bytes, B, H, T, d,
+                                scale, mode, lo, hi, None)
+
+
+def test_decode_range_workspace_bytes(lib):
+    # the range's chunks of C positions: ceil((hi - lo) / C) per (b, h)
+    for d, C in ((64, 254), (128, 126), (256, 62)):
+        for lo, hi in ((0, 1), (0, C), (0, C + 1), (2, 2 + C), (500, 8193)):
+            n = -(-(hi - lo) // C)
+            assert lib.csa_decode_range_workspace_bytes(3, 5, lo, hi, d) == 15 * n * (d + 2) * 4
+        # a range over all positions needs what csa_decode needs
+        assert (lib.csa_decode_range_workspace_bytes(2, 3, 0, 8193, d)
+                == lib.csa_decode_workspace_bytes(2, 3, 8192, d))
+    assert lib.csa_decode_range_workspace_bytes(1, 1, 5, 4, 64) == -1
+    assert lib.csa_decode_range_workspace_bytes(1, 1, -1, 4, 64) == -1
+    assert lib.csa_decode_range_workspace_bytes(1, 1, 0, 4, 96) == -1
+
+
+def test_decode_range_validation(lib):
+    assert dec_range(lib, lo=1, hi=100) == L.CSA_ERR_INVALID_ARG  # right after the sink
+    assert dec_range(lib, lo=-1) == L.CSA_ERR_INVALID_ARG
+    assert dec_range(lib, lo=100, hi=100) == L.CSA_ERR_INVALID_ARG
+    assert dec_range(lib, lo=0, hi=302) == L.CSA_ERR_INVALID_ARG  # positions 0..T only
+    assert dec_range(lib, lse=NULL) == L.CSA_ERR_INVALID_ARG  # the merge needs lse
+    assert dec_range(lib, q=NULL) == L.CSA_ERR_INVALID_ARG
+    assert dec_range(lib, ws_bytes=16) == L.CSA_ERR_INVALID_ARG
+    assert dec_range(lib, mode=2) == L.CSA_ERR_INVALID_ARG
+    assert dec_range(lib, d=96) == L.CSA_ERR_UNSUPPORTED
+    assert dec_range(lib, out=ctypes.c_void_p(4104)) == L.CSA_ERR_ALIGNMENT
+    assert dec_range(lib, k=NULL, v=NULL, q=NULL, out=NULL, lse=NULL, ws=NULL, B=0) == L.CSA_OK
+    m = lambda **kw: lib.csa_decode_merge_ranges(kw.get("o", FAKE), kw.get("l", FAKE),
+                                                 kw.get("R", 2), 2, 2, kw.get("d", 128),
+                                                 kw.get("out", FAKE), NULL, None)
+    assert m(R=0) == L.CSA_ERR_INVALID_ARG
+    assert m(d=300) == L.CSA_ERR_INVALID_ARG
+    assert m(o=NULL) == L.CSA_ERR_INVALID_ARG
+    assert m(out=ctypes.c_void_p(4097)) == L.CSA_ERR_ALIGNMENT
+    import torch
+
+    if not torch.cuda.is_available():
+        assert dec_range(lib) == L.CSA_ERR_NO_DEVICE
+        assert m() == L.CSA_ERR_NO_DEVICE
+
+
 def bwd(lib, *, q=FAKE, k=FAKE, v=FAKE, k0=NULL, v0=NULL, out=FAKE, lse=FAKE, dout=FAKE,
         dq=FAKE, dk=FAKE, dv=FAKE, dk0=NULL, dv0=NULL, ws=FAKE, ws_bytes=1 << 30, B=1, H=2, T=8,
         d=64, scale=0.1, mode=0):

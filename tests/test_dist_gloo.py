@@ -208,3 +208,91 @@ def test_decode_two_gloo_ranks(mode):
     ro, rl = _oracle_decode(x["q"].float(), x["k"].float(), x["v"].float(), x["k0"].float(),
                             x["v0"].float(), x["seqlens"], mode, 0.4)
     assert np.array_equal(o, ro.numpy()) and np.array_equal(lse, rl.numpy())
+
+
+# ---------------------------------------------------------------- context parallelism
+def _merge_np(o_parts, lse_parts):
+    """lse-weighted merge of range partials (test-side, float64)."""
+    lses = lse_parts.double()
+    L = lses.max(dim=0).values
+    w = torch.exp(lses - L)
+    o = (w[..., None] * o_parts.double()).sum(dim=0) / w.sum(dim=0)[..., None]
+    return o, L + torch.log(w.sum(dim=0))
+
+
+def _cp_worker(rank, world, port, mode, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import oracle
+        from continuous_softmax_attention_gb300.dist import (cache_shard, context_ranges,
+                                                             decode_context_parallel)
+        from continuous_softmax_attention_gb300.inputs import make_decode_inputs
+
+        x = make_decode_inputs(3, 2, 60, 8, seed=9, len_lo=1)
+        T = x["k"].shape[2]
+        lo, hi = context_ranges(T, world)[rank]
+        ks, vs = cache_shard(x["k"], x["v"], lo, hi)
+
+        def partial(qq, k_shard, v_shard, TT, a, b, k0, v0, *, seqlens, mode, scale):
+            # the oracle stands in for csa_decode_range (it reads the whole cache)
+            assert (a, b) == (lo, hi) and k_shard.shape[2] == ks.shape[2] and TT == T
+            o, lse = oracle.decode_range(qq, x["k"], x["v"], seqlens, a, b, k0, v0, scale=scale,
+                                         mode=mode)
+            return torch.from_numpy(o), torch.from_numpy(lse)
+
+        o, lse = decode_context_parallel(x["q"], ks, vs, T, x["k0"], x["v0"],
+                                         seqlens=x["seqlens"], mode=mode, scale=0.7, fn=partial,
+                                         merge_fn=_merge_np)
+        q.put((rank, o.numpy(), lse.numpy()))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,mode", [(2, 0), (3, 1), (3, 2)])
+def test_decode_context_parallel_gloo(world, mode):
+    """The cache split along time over 2 or 3 ranks: each rank's partial over
+    its positions, one all-gather, the lse-weighted merge; every rank ends
+    with the whole decode step."""
+    from continuous_softmax_attention_gb300.inputs import make_decode_inputs
+
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_cp_worker, args=(r, world, port, mode, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    x = make_decode_inputs(3, 2, 60, 8, seed=9, len_lo=1)
+    ro, rl = _oracle_decode(x["q"].float(), x["k"].float(), x["v"].float(), x["k0"].float(),
+                            x["v0"].float(), x["seqlens"], mode, 0.7)
+    for _, o, lse in got:
+        assert np.abs(o - ro.numpy()).max() < 1e-9
+        assert np.abs(lse - rl.numpy()).max() < 1e-9
+
+
+def test_context_ranges_and_shards():
+    from continuous_softmax_attention_gb300.dist import cache_shard, context_ranges
+
+    for T in (3, 7, 60, 125, 126, 127, 8192):
+        for world in range(1, min(8, (T + 1) // 2) + 1):
+            rs = context_ranges(T, world)
+            assert rs[0][0] == 0 and rs[-1][1] == T + 1 and len(rs) == world
+            assert all(a < b for a, b in rs)
+            assert all(b1 == a2 for (_, b1), (a2, _) in zip(rs, rs[1:]))
+            assert all(a != 1 for a, _ in rs)  # never right after the sink
+    with pytest.raises(ValueError):
+        context_ranges(2, 2)
+    k = torch.arange(2 * 1 * 10 * 4, dtype=torch.float32).reshape(2, 1, 10, 4)
+    for lo, hi in ((0, 4), (4, 8), (8, 11), (2, 3)):
+        ks, vs = cache_shard(k, k, lo, hi)
+        r0, r1 = max(lo - 2, 0), min(hi, 10)
+        assert torch.equal(ks, k[:, :, r0:r1]) and ks.is_contiguous()
+        # the rows of the range's positions and of its two neighbours
+        need = {p - 1 for p in range(max(lo - 1, 1), min(hi + 1, 11))}
+        assert need == set(range(r0, r1))
