@@ -18,6 +18,8 @@
 //   4. writes the partial sums l = sum w and o = sum w v, with m.
 // A second kernel merges the chunks of each (b, h): with M the largest m,
 // o = sum_c 2^{m_c-M} o_c / sum_c 2^{m_c-M} l_c and lse = (M + log2 L) ln 2.
+// It is launched as a programmatic dependent of the first, so that its launch
+// overlaps the first kernel's tail; it waits for the partials before reading.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -363,6 +365,9 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecPa
     __shared__ float part[kParts][D];
     const int bh = blockIdx.x, b = bh / p.H, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = p.seqlens ? p.seqlens[b] : p.T;
+    // launched as a programmatic dependent of the chunk kernel: wait until its
+    // partials are complete and visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     auto store = [&](int col, float val) {
         if (p.out_f32)
             p.out_f32[(size_t)bh * D + col] = val;
@@ -465,7 +470,16 @@ int launch_decode(DecParams p, cudaStream_t stream) {
         cudaSuccess)
         return CSA_ERR_CUDA;
     kern<<<(unsigned)grid, kThreads, Cf::kSmemBytes, stream>>>(p);
-    decode_merge_kernel<D><<<(unsigned)BH, kMergeThreads, 0, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)BH);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, p) != cudaSuccess) return CSA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }
 
