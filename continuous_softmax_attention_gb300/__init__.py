@@ -8,6 +8,7 @@ loudly when the library has not been built.
 from .inputs import ZERO, COPY_FIRST, GIVEN  # noqa: F401
 from ._lib import (  # noqa: F401
     CsaError,
+    HostForwardPipeline,
     backward,
     backward_workspace_bytes,
     decode,
@@ -30,7 +31,7 @@ from ._lib import (  # noqa: F401
 )
 
 __all__ = [
-    "ZERO", "COPY_FIRST", "GIVEN", "CsaError", "forward", "forward_host",
+    "ZERO", "COPY_FIRST", "GIVEN", "CsaError", "forward", "forward_host", "HostForwardPipeline",
     "forward_host_workspace_bytes", "forward_symmetric", "std_forward",
     "backward",
     "backward_workspace_bytes", "decode", "decode_noalloc", "decode_workspace_bytes",

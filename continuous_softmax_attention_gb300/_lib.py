@@ -65,7 +65,9 @@ def load():
                        ("csa_decode_merge_ranges", [p, p, i, i, i, i, p, p, p]),
                        ("csa_backward", bwd), ("csa_backward_f32", bwd),
                        ("csa_forward_host", [p, p, p, p, p, p, p, p, ctypes.c_longlong, i, i, i,
-                                             i, f, i, i, p, p, p])):
+                                             i, f, i, i, p, p, p]),
+                       ("csa_forward_host_ex", [p, p, p, p, p, p, p, p, ctypes.c_longlong, i, i,
+                                                i, i, f, i, i, u, p, p, p])):
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = i
@@ -174,16 +176,22 @@ def forward_host_workspace_bytes(B: int, H: int, T: int, d: int) -> int:
     return n
 
 
+CSA_HOST_NO_ENTRY_WAIT = 1
+
+
 def forward_host(q, k, v, out, lse=None, k0=None, v0=None, *, mode: int = 0, scale=None,
                  workspace=None, heads_per_chunk: int = 4, stream=None, stream_h2d=None,
-                 stream_d2h=None):
+                 stream_d2h=None, no_entry_wait: bool = False):
     """csa_forward from host tensors, end to end, with the copies overlapped.
 
     q, k, v, out: CPU bf16 [B, H, T, d] (pinned for the overlap); lse: CPU
     float32 [B, H, T] or None; k0, v0: CUDA [H, d] in mode GIVEN.
     workspace: CUDA uint8 tensor of forward_host_workspace_bytes(...) bytes.
     The call is asynchronous: out and lse are ready once `stream` (torch's
-    current stream by default) has reached this point."""
+    current stream by default) has reached this point.  no_entry_wait: the
+    copies in do not wait for work already queued on `stream`
+    (csa_forward_host_ex with CSA_HOST_NO_ENTRY_WAIT); the caller orders the
+    calls that share a workspace."""
     import torch
 
     B, H, T, d = q.shape
@@ -208,11 +216,49 @@ def forward_host(q, k, v, out, lse=None, k0=None, v0=None, *, mode: int = 0, sca
     cs = _stream_handle(stream)
     hs = _stream_handle(stream_h2d) if stream_h2d is not None else cs
     ds = _stream_handle(stream_d2h) if stream_d2h is not None else cs
-    _check(load().csa_forward_host(_ptr(q), _ptr(k), _ptr(v), _ptr(k0), _ptr(v0), _ptr(out),
-                                   _ptr(lse), _ptr(workspace), nbytes, B, H, T, d, float(scale),
-                                   int(mode), int(heads_per_chunk), cs, hs, ds),
-           "csa_forward_host")
+    flags = CSA_HOST_NO_ENTRY_WAIT if no_entry_wait else 0
+    _check(load().csa_forward_host_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(k0), _ptr(v0), _ptr(out),
+                                      _ptr(lse), _ptr(workspace), nbytes, B, H, T, d,
+                                      float(scale), int(mode), int(heads_per_chunk), flags, cs,
+                                      hs, ds),
+           "csa_forward_host_ex")
     return out, lse
+
+
+class HostForwardPipeline:
+    """Back-to-back forward_host calls that overlap across calls: two
+    workspaces used alternately, each call's copies in (CSA_HOST_NO_ENTRY_WAIT)
+    waiting only for the call before last, which used the same workspace, to
+    have completed on `stream`.  So one call's copies in run while the previous
+    call's kernels and copies out do.  Stream and event plumbing only."""
+
+    def __init__(self, B: int, H: int, T: int, d: int, device, *, heads_per_chunk: int = 4,
+                 stream=None):
+        import torch
+
+        n = forward_host_workspace_bytes(B, H, T, d)
+        self.ws = [torch.empty(max(n, 16), dtype=torch.uint8, device=device) for _ in range(2)]
+        self.done = [None, None]
+        self.s_h2d = torch.cuda.Stream(device=device)
+        self.s_d2h = torch.cuda.Stream(device=device)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(device)
+        self.heads_per_chunk = heads_per_chunk
+        self.calls = 0
+
+    def __call__(self, q, k, v, out, lse=None, k0=None, v0=None, *, mode: int = 0, scale=None):
+        import torch
+
+        w = self.calls & 1
+        if self.done[w] is not None:
+            self.s_h2d.wait_event(self.done[w])
+        forward_host(q, k, v, out, lse, k0, v0, mode=mode, scale=scale, workspace=self.ws[w],
+                     heads_per_chunk=self.heads_per_chunk, stream=self.stream,
+                     stream_h2d=self.s_h2d, stream_d2h=self.s_d2h, no_entry_wait=True)
+        ev = torch.cuda.Event()
+        ev.record(self.stream)
+        self.done[w] = ev
+        self.calls += 1
+        return out, lse
 
 
 def std_forward(q, k, v, *, scale=None, out=None, lse=None, stream=None, want_lse: bool = True,

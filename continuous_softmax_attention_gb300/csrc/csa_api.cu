@@ -234,10 +234,12 @@ long long csa_forward_host_workspace_bytes(int B, int H, int T, int d) {
     return csa_host_scratch_bytes(B, H, T, d);
 }
 
-int csa_forward_host(const void *q, const void *k, const void *v, const void *k0, const void *v0,
-                     void *out, float *lse, void *workspace, long long workspace_bytes, int B,
-                     int H, int T, int d, float scale, int k0_mode, int heads_per_chunk,
-                     csa_stream_t stream, csa_stream_t stream_h2d, csa_stream_t stream_d2h) {
+int csa_forward_host_ex(const void *q, const void *k, const void *v, const void *k0,
+                        const void *v0, void *out, float *lse, void *workspace,
+                        long long workspace_bytes, int B, int H, int T, int d, float scale,
+                        int k0_mode, int heads_per_chunk, unsigned flags, csa_stream_t stream,
+                        csa_stream_t stream_h2d, csa_stream_t stream_d2h) {
+    if (flags & ~CSA_HOST_NO_ENTRY_WAIT) return CSA_ERR_INVALID_ARG;
     bool empty;
     int rc = check_common(q, k, v, k0, v0, out, B, H, T, d, scale, k0_mode, true, &empty);
     if (rc != CSA_OK || empty) return rc;
@@ -252,9 +254,19 @@ int csa_forward_host(const void *q, const void *k, const void *v, const void *k0
     if ((d == 64 || d == 128) && scale < 0.0f) return CSA_ERR_UNSUPPORTED;
     if ((rc = device_ok()) != CSA_OK) return rc;
     return csa_host_forward(q, k, v, k0, v0, out, lse, workspace, B, H, T, d, scale, k0_mode,
-                            heads_per_chunk, reinterpret_cast<cudaStream_t>(stream),
+                            heads_per_chunk, !(flags & CSA_HOST_NO_ENTRY_WAIT),
+                            reinterpret_cast<cudaStream_t>(stream),
                             reinterpret_cast<cudaStream_t>(stream_h2d),
                             reinterpret_cast<cudaStream_t>(stream_d2h));
+}
+
+int csa_forward_host(const void *q, const void *k, const void *v, const void *k0, const void *v0,
+                     void *out, float *lse, void *workspace, long long workspace_bytes, int B,
+                     int H, int T, int d, float scale, int k0_mode, int heads_per_chunk,
+                     csa_stream_t stream, csa_stream_t stream_h2d, csa_stream_t stream_d2h) {
+    return csa_forward_host_ex(q, k, v, k0, v0, out, lse, workspace, workspace_bytes, B, H, T, d,
+                               scale, k0_mode, heads_per_chunk, 0u, stream, stream_h2d,
+                               stream_d2h);
 }
 
 long long csa_decode_range_workspace_bytes(int B, int H, int pos_lo, int pos_hi, int d) {

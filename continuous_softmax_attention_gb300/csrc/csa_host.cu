@@ -42,8 +42,8 @@ long long csa_host_scratch_bytes(int B, int H, int T, int d) {
 
 int csa_host_forward(const void *q_h, const void *k_h, const void *v_h, const void *k0,
                      const void *v0, void *out_h, float *lse_h, void *scratch, int B, int H, int T,
-                     int d, float scale, int mode, int heads_per_chunk, cudaStream_t s_compute,
-                     cudaStream_t s_h2d, cudaStream_t s_d2h) {
+                     int d, float scale, int mode, int heads_per_chunk, bool entry_wait,
+                     cudaStream_t s_compute, cudaStream_t s_h2d, cudaStream_t s_d2h) {
     const long long rows = (long long)B * H * T;
     const long long tensor = (rows * d * 2 + 255) / 256 * 256;
     uint8_t *base = static_cast<uint8_t *>(scratch);
@@ -53,13 +53,16 @@ int csa_host_forward(const void *q_h, const void *k_h, const void *v_h, const vo
     const size_t chunk_bytes = chunk_rows * d * 2;
     const int chunks_per_b = H / heads_per_chunk;
     Events evs;
-    // the copies of this call must not overtake work still queued on the
-    // compute stream (a previous call reading the same device buffers)
-    cudaEvent_t start = evs.make();
-    if (!start || cudaEventRecord(start, s_compute) != cudaSuccess ||
-        cudaStreamWaitEvent(s_h2d, start, 0) != cudaSuccess ||
-        cudaStreamWaitEvent(s_d2h, start, 0) != cudaSuccess)
-        return CSA_ERR_CUDA;
+    // The copies of this call must not overtake work still queued on the
+    // compute stream (a previous call reading the same device buffers),
+    // unless the caller orders calls that share a workspace itself.
+    if (entry_wait) {
+        cudaEvent_t start = evs.make();
+        if (!start || cudaEventRecord(start, s_compute) != cudaSuccess ||
+            cudaStreamWaitEvent(s_h2d, start, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(s_d2h, start, 0) != cudaSuccess)
+            return CSA_ERR_CUDA;
+    }
     cudaEvent_t last_back = nullptr;
     for (int b = 0; b < B; ++b) {
         for (int c = 0; c < chunks_per_b; ++c) {

@@ -84,9 +84,11 @@ int csa_tc_backward(const void *q, const void *k, const void *v, const void *k0,
 int csa_tc_backward_take_status(void);
 
 // End-to-end forward from host buffers (csa_host.cu), pipelined over chunks
-// of heads_per_chunk heads on three streams.
+// of heads_per_chunk heads on three streams.  entry_wait: the copies wait for
+// the work already queued on s_compute (false: the caller orders calls that
+// share a workspace).
 long long csa_host_scratch_bytes(int B, int H, int T, int d);
 int csa_host_forward(const void *q_h, const void *k_h, const void *v_h, const void *k0,
                      const void *v0, void *out_h, float *lse_h, void *scratch, int B, int H, int T,
-                     int d, float scale, int mode, int heads_per_chunk, cudaStream_t s_compute,
-                     cudaStream_t s_h2d, cudaStream_t s_d2h);
+                     int d, float scale, int mode, int heads_per_chunk, bool entry_wait,
+                     cudaStream_t s_compute, cudaStream_t s_h2d, cudaStream_t s_d2h);

@@ -129,6 +129,25 @@ int csa_forward_host(const void *q, const void *k, const void *v, const void *k0
                      int H, int T, int d, float scale, int k0_mode, int heads_per_chunk,
                      csa_stream_t stream, csa_stream_t stream_h2d, csa_stream_t stream_d2h);
 
+/*
+ * csa_forward_host_ex - csa_forward_host with flags (the pages have no
+ *   counterpart).  flags = 0 is csa_forward_host.  CSA_HOST_NO_ENTRY_WAIT:
+ *   the host-to-device copies do not wait for the work already queued on
+ *   `stream`, so that a call's copies in can overlap the previous call's
+ *   kernels and copies out.  The caller then orders the calls that share a
+ *   workspace itself: a call's copies in must not start before the previous
+ *   call on the same workspace has completed on `stream` (for instance: two
+ *   workspaces used alternately, each call recording an event on `stream`
+ *   after it, and stream_h2d waiting for the event of the call before last).
+ *   Unknown flag bits: CSA_ERR_INVALID_ARG.  Otherwise as csa_forward_host.
+ */
+#define CSA_HOST_NO_ENTRY_WAIT 1u
+int csa_forward_host_ex(const void *q, const void *k, const void *v, const void *k0,
+                        const void *v0, void *out, float *lse, void *workspace,
+                        long long workspace_bytes, int B, int H, int T, int d, float scale,
+                        int k0_mode, int heads_per_chunk, unsigned flags, csa_stream_t stream,
+                        csa_stream_t stream_h2d, csa_stream_t stream_d2h);
+
 /* csa_forward_host_workspace_bytes - device workspace csa_forward_host needs
  * (host only), or -1 for a negative size or d outside 1..256. */
 long long csa_forward_host_workspace_bytes(int B, int H, int T, int d);

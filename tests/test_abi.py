@@ -220,7 +220,14 @@ def test_forward_host_validation(lib):
     assert call(ws_bytes=need - 1) == L.CSA_ERR_INVALID_ARG
     assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == L.CSA_ERR_ALIGNMENT
     assert call(q=NULL) == L.CSA_ERR_INVALID_ARG
+    ex = lambda flags: lib.csa_forward_host_ex(
+        FAKE, FAKE, FAKE, None, None, FAKE, None, ctypes.c_void_p(1 << 20), need, 1, 4, 16, 64,
+        ctypes.c_float(0.1), 0, 2, flags, None, None, None)
+    assert ex(2) == L.CSA_ERR_INVALID_ARG  # unknown flag bit
+    assert ex(0x80000000) == L.CSA_ERR_INVALID_ARG
     import torch
 
     if not torch.cuda.is_available():
         assert call() == L.CSA_ERR_NO_DEVICE
+        assert ex(0) == L.CSA_ERR_NO_DEVICE
+        assert ex(L.CSA_HOST_NO_ENTRY_WAIT) == L.CSA_ERR_NO_DEVICE

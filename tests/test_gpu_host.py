@@ -76,3 +76,29 @@ def test_host_path_rejects_bad_chunks():
     for hpc in (0, 3, 5):
         with pytest.raises(CsaError):
             forward_host(x["q"], x["k"], x["v"], out, workspace=ws, heads_per_chunk=hpc)
+
+
+def test_back_to_back_calls_overlapped_across_calls():
+    """Five calls in a row, each on different inputs, through the two-workspace
+    pipeline (copies in without the entry wait): every result must still equal
+    the device path bit for bit, so no call overwrote a workspace or an output
+    another call was still using."""
+    from continuous_softmax_attention_gb300 import HostForwardPipeline
+
+    B, H, T, d = 1, 8, 640, 128
+    pipe = HostForwardPipeline(B, H, T, d, "cuda", heads_per_chunk=2)
+    runs = []
+    for i in range(5):
+        x = make_inputs(B, H, T, d, "bf16", seed=900 + i)
+        out = torch.empty(B, H, T, d, dtype=torch.bfloat16).pin_memory()
+        lse = torch.empty(B, H, T).pin_memory()
+        # the pinned inputs stay referenced until the copies have run
+        hq, hk, hv = pinned(x["q"]), pinned(x["k"]), pinned(x["v"])
+        pipe(hq, hk, hv, out, lse, mode=0)
+        runs.append((x, out, lse, (hq, hk, hv)))
+    torch.cuda.current_stream().synchronize()
+    for x, out, lse, _ in runs:
+        g = {k: t.cuda() for k, t in x.items()}
+        ro, rl = forward(g["q"], g["k"], g["v"], mode=0)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ro.cpu()) and torch.equal(lse, rl.cpu())
