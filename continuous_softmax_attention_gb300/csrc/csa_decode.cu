@@ -6,7 +6,8 @@
 // The step reads every cached key and value once and does about two flops
 // per byte read, so it is bound by HBM bandwidth and runs on CUDA cores.
 // The key positions 0..n (0 is the sink k_0, position i >= 1 is cache row
-// i - 1) are cut into chunks of C positions.  One CTA per (b, h, chunk):
+// i - 1) are cut into chunks of C positions (126 at d = 128, 254 at d = 64,
+// 110 at d = 256).  One CTA per (b, h, chunk):
 //   1. stages the chunk's keys plus one halo key on each side (the correction
 //      b of a key needs both neighbours' logits, eq. (10)) and the chunk's
 //      values, with two bulk asynchronous copies on separate barriers, so
@@ -58,7 +59,10 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 
 template <int D>
 struct DecCfg {
-    static constexpr int KRows = 16384 / D;  // keys staged (32 KiB): the chunk and a halo key each side
+    // keys staged: the chunk and a halo key each side (32 KiB, three CTAs per
+    // SM; at d = 256, 56 KiB and two CTAs per SM, which measured faster than
+    // 32 KiB chunks of only 62 positions)
+    static constexpr int KRows = D == 256 ? 112 : 16384 / D;
     static constexpr int C = KRows - 2;      // positions per chunk
     static constexpr int LPK = D / 8;        // lanes per key, 16 bytes (8 columns) each
     static constexpr int NGrp = kThreads / LPK;  // lane groups in the block
@@ -72,7 +76,7 @@ struct DecCfg {
     static_assert(kOffV % 16 == 0 && kOffA % 16 == 0, "bulk copy destinations 16-byte aligned");
     static_assert(NGrp * D * 4 <= KRows * D * 2, "value partials fit in the key buffer");
     static_assert(KRows % (2 * NGrp) == 0, "the logit loop has no idle lanes");
-    static_assert(kSmemBytes <= 75 * 1024, "three CTAs per SM");
+    static_assert(kSmemBytes <= (D == 256 ? 113 : 75) * 1024, "three CTAs per SM (two at d = 256)");
 };
 
 struct DecParams {

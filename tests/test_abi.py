@@ -101,9 +101,9 @@ def dec(lib, *, q=FAKE, k=FAKE, v=FAKE, k0=NULL, v0=NULL, seqlens=NULL, out=FAKE
 
 
 def test_decode_workspace_bytes(lib):
-    # one chunk of C = 16384/d - 2 positions per CTA over positions 0..T, each
+    # one chunk of C positions (16384/d - 2; 110 at d = 256) per CTA over positions 0..T, each
     # leaving d partial outputs plus (max, sum): B*H*(T//C + 1)*(d + 2) floats
-    for d, C in ((64, 254), (128, 126), (256, 62)):
+    for d, C in ((64, 254), (128, 126), (256, 110)):
         for T in (1, C - 1, C, C + 1, 8192):
             assert lib.csa_decode_workspace_bytes(3, 5, T, d) == 15 * (T // C + 1) * (d + 2) * 4
     assert lib.csa_decode_workspace_bytes(0, 5, 10, 64) == 0
@@ -141,7 +141,7 @@ def dec_range(lib, *, q=FAKE, k=FAKE, v=FAKE, k0=NULL, v0=NULL, seqlens=NULL, ou
 
 def test_decode_range_workspace_bytes(lib):
     # the range's chunks of C positions: ceil((hi - lo) / C) per (b, h)
-    for d, C in ((64, 254), (128, 126), (256, 62)):
+    for d, C in ((64, 254), (128, 126), (256, 110)):
         for lo, hi in ((0, 1), (0, C), (0, C + 1), (2, 2 + C), (500, 8193)):
             n = -(-(hi - lo) // C)
             assert lib.csa_decode_range_workspace_bytes(3, 5, lo, hi, d) == 15 * n * (d + 2) * 4
