@@ -591,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // flight while chunk kk is computed
             uint32_t a[16], g[16], an[1] = {0u}, gn[1] = {0u};
             const int cb = 64 * half;
+            uint32_t hP[8], hS[8];  // chunk 0's P and dS while they are held (d = 128)
             // this row's 16 keys from column c0 = 16-byte chunks ch, ch+1 of box c0/64
             auto store_pds = [&](int c0, const uint32_t (&qP)[8], const uint32_t (&qS)[8]) {
                 const int box = c0 >> 6, ch = (c0 & 63) >> 3;
@@ -644,13 +645,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   Lc, Fc, pP, pS);
                 // P and dS overwrite the previous tile's staged dQ_part: wait until
                 // its reductions have read it (the MMAs reading the previous P
-                // and dS finished before this tile's S and dP did)
-                if (kk == 0 && j > 0 &&
+                // and dS finished before this tile's S and dP did).  At d = 128,
+                // where those reductions take longest, chunk 0's P and dS are held
+                // in registers and stored after chunk 1, so the wait comes later.
+                constexpr int kFirstStore = D == 128 ? 1 : 0;
+                if (kFirstStore == 1 && kk == 0) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        hP[i] = pP[i];
+                        hS[i] = pS[i];
+                    }
+                    continue;
+                }
+                if (kk == kFirstStore && j > 0 &&
                     !__all_sync(0xffffffffu, wait_b(BAR(C::kBarStageFree), (j - 1) & 1, abort_flag))) {
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");  // chunk 1's loads
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");  // the next chunk's loads
                     ok = false;
                     break;
                 }
+                if (kFirstStore == 1 && kk == 1) store_pds(cb, hP, hS);
                 store_pds(c0, pP, pS);
             }
             if (!ok) break;
