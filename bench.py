@@ -9,9 +9,10 @@ events on the launching stream and the steps are summed.
 
 Also reported on the same JSON line:
   e2e          the same metric through the C ABI with host buffers
-               (csa_forward_host): pinned host -> device copies of q, k, v,
-               the kernel, and the device -> host copy of o and lse, all
-               inside the timed region, overlapped by chunks of 4 heads
+               (csa_forward_host_ex): pinned host -> device copies of q, k,
+               v, the kernels, and the device -> host copy of o and lse, all
+               inside the timed region, overlapped by chunks of 8 heads and,
+               through two alternating workspaces, across consecutive steps
   std          the library's standard causal attention kernel (eq. (12)) at
                the same shape, and the ratio continuous / standard
   roofline     tensor-core bound: algorithmic matmul flops / kernel time
@@ -26,6 +27,10 @@ Also reported on the same JSON line:
                against the measured copy bandwidth, plus its own e2e (the
                queries from pinned host memory, outputs back to the host;
                the cache stays resident as it would while serving)
+  backward     the backward pass (csa_backward) at the same shape
+  workloads    the continuous and standard kernels at the mid (4 x 16 x
+               2048 x 128, RoPE) and long (1 x 8 x 32768 x 64, per-head
+               sink) workloads
 
 `--impl reference` times the CPU oracle alone (the reference arm).
 Multi-GPU (torchrun): every rank runs its own copy of the workload (the
@@ -224,6 +229,7 @@ def run_gpu(args):
     std_call = lambda: csa.std_forward(g["q"], g["k"], g["v"], scale=scale, out=out, lse=lse)
 
     dec = None if args.no_decode else DecodeBench(csa, dev, stream, flush)
+    more = None if args.no_workloads else WorkloadBench(csa, dev)
     bwd = None if args.no_backward else BackwardBench(csa, g, out, lse, scale, w.modes[0], dev)
 
     # end to end through the C ABI with host buffers (csa_forward_host_ex: the
@@ -267,6 +273,8 @@ def run_gpu(args):
             dec.e2e_call()
         if bwd is not None:
             bwd.call()
+        if more is not None:
+            more.warm()
     torch.cuda.synchronize()
     assert csa.device_status() == 0
 
@@ -283,6 +291,8 @@ def run_gpu(args):
             dec.ms_e2e = timed(dec.e2e_call, args.decode_steps)
         if bwd is not None:
             bwd.ms = timed(bwd.call, args.backward_steps)
+        if more is not None:
+            more.time(timed, args.workload_steps)
     barrier()
     t_wall = time.perf_counter() - t_wall
     status = csa.device_status()
@@ -299,6 +309,8 @@ def run_gpu(args):
         dec.tot, dec.tot_e2e = total(dec.ms), total(dec.ms_e2e)
     if bwd is not None:
         bwd.tot = total(bwd.ms)
+    if more is not None:
+        more.reduce(total)
     if ws > 1:
         dist.destroy_process_group()
     if rank != 0:
@@ -347,7 +359,8 @@ def run_gpu(args):
                               "B*H*T(T+1)/2 pairs (no sink)"},
         "gpu_launches": 4 * K + K * (B * H // E2E_HEADS_PER_CHUNK) +
                         (0 if dec is None else 2 * 2 * args.decode_steps) +
-                        (0 if bwd is None else bwd.launches * args.backward_steps),
+                        (0 if bwd is None else bwd.launches * args.backward_steps) +
+                        (0 if more is None else more.launches * args.workload_steps),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": burst,
                      "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
                      "peak_source": f"{src} bf16 dense (burst)", "traffic": recorded_traffic(),
@@ -361,6 +374,8 @@ def run_gpu(args):
         line["decode"] = dec.summary(ws, args.decode_steps)
     if bwd is not None:
         line["backward"] = bwd.summary(ws, args.backward_steps, burst, src)
+    if more is not None:
+        line["workloads"] = more.summary(ws, args.workload_steps, burst, src)
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = cpu_baseline(x, scale, budget_s=args.cpu_seconds)
         line["short_conv"]["cpu_baseline"] = cpu_baseline_form(x, scale, "short_conv")
@@ -370,6 +385,73 @@ def run_gpu(args):
         if dec is not None:
             line["decode"]["cpu_baseline"] = cpu_baseline_decode(dec)
     return line
+
+
+class WorkloadBench:
+    """The forward pass and the standard kernel at the two other timed shapes
+    of the evaluation plan: mid (B=4, H=16, T=2048, d=128, RoPE, zero sink)
+    and long (B=1, H=8, T=32768, d=64, per-head sink).  Their parity tests
+    run the same launches; this puts their throughput on the same line."""
+
+    NAMES = ("mid", "long")
+
+    def __init__(self, csa, dev):
+        import torch
+
+        from continuous_softmax_attention_gb300.inputs import (WORKLOADS, algorithmic_flops,
+                                                               workload_inputs)
+        self.legs = []
+        for name in self.NAMES:
+            w = WORKLOADS[name]
+            g = {k: t.to(dev) for k, t in workload_inputs(name).items()}
+            scale = 1.0 / math.sqrt(w.d)
+            out = torch.empty_like(g["q"])
+            lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
+            mode = w.modes[0]
+            cont = (lambda g=g, mode=mode, scale=scale, out=out, lse=lse:
+                    csa.forward(g["q"], g["k"], g["v"], g["k0"], g["v0"], mode=mode, scale=scale,
+                                out=out, lse=lse))
+            std = (lambda g=g, scale=scale, out=out, lse=lse:
+                   csa.std_forward(g["q"], g["k"], g["v"], scale=scale, out=out, lse=lse))
+            self.legs.append({"name": name, "w": w, "mode": mode, "calls": (cont, std),
+                              "flops": (algorithmic_flops(w.B, w.H, w.T, w.d, continuous=True),
+                                        algorithmic_flops(w.B, w.H, w.T, w.d, continuous=False)),
+                              "bytes": 3 * g["q"].numel() * 2})
+        self.launches = 2 * len(self.legs)
+
+    def warm(self):
+        for leg in self.legs:
+            for c in leg["calls"]:
+                c()
+
+    def time(self, timed, steps):
+        for leg in self.legs:
+            leg["ms"] = [timed(c, steps) for c in leg["calls"]]
+
+    def reduce(self, total):
+        for leg in self.legs:
+            leg["tot"] = [total(ms) for ms in leg["ms"]]
+
+    def summary(self, world, steps, peak, src):
+        out = {}
+        for leg in self.legs:
+            w = leg["w"]
+            (fc, fs), (tc, ts) = leg["flops"], leg["tot"]
+            vc = world * fc * steps / (tc * 1e-3) / 1e12
+            vs = world * fs * steps / (ts * 1e-3) / 1e12
+            out[leg["name"]] = {
+                "config": {"B": w.B, "H": w.H, "T": w.T, "d": w.d,
+                           "k0_mode": ("zero", "copy_first", "given")[leg["mode"]],
+                           "rope": bool(w.rope)},
+                "value": round(vc, 3), "unit": UNIT, "ms_per_step": round(tc / steps, 5),
+                "pct_bf16_peak": round(100.0 * (fc / (tc / steps * 1e-3) / 1e12) / peak, 2),
+                "peak_source": f"{src} bf16 dense (burst)",
+                "std": {"value": round(vs, 3), "ms_per_step": round(ts / steps, 5)},
+                "ratio_continuous_over_std": round(vc / vs, 4),
+                "l2": (f"flushed (512 MiB write) before every timed step; q, k, v "
+                       f"{leg['bytes'] / 2**20:.0f} MiB"),
+            }
+        return out
 
 
 class BackwardBench:
@@ -683,6 +765,9 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode workload")
     ap.add_argument("--backward-steps", type=int, default=50, help="timed steps of the backward pass")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward pass")
+    ap.add_argument("--workload-steps", type=int, default=20,
+                    help="timed steps of each kernel at the mid and long workloads")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the mid and long workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
