@@ -51,6 +51,7 @@
 // time; on expiry the kernel records CSA_ERR_TIMEOUT, every role skips its
 // remaining work, the MMA issuer waits for its own MMAs, the producer waits
 // for its own copies, and TMEM is freed.
+#include <mutex>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -97,13 +98,18 @@ struct TcCfg {
     static constexpr int kBarODone = kBarPFull + 1;
     static constexpr int kBarDrain = kBarODone + 1;
     static constexpr int kBarX = kBarDrain + 1;  // half-to-half exchange
-    static constexpr int kNumBars = kBarX + 1;
+    static constexpr int kBarQEmpty = kBarX + 1;     // an item's last S is done
+    static constexpr int kBarQRead = kBarQEmpty + 1;  // its sink logits are read from Q
+    static constexpr int kBarItemFull = kBarQRead + 1;    // [2] item ring
+    static constexpr int kBarItemEmpty = kBarItemFull + 2;  // [2]
+    static constexpr int kNumBars = kBarItemEmpty + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     // exchange buffers between the two column halves of the query tile:
     //   xmax   [2 slots][2 halves][128 rows]  partial row maxima
     //   xcarry [2 slots][128 rows]            L share carried to the next tile
     //   xfin   [2 halves][128 rows][2]        final fp32 sum, sink weight
-    static constexpr int kOffXMax = kOffMisc + 16;
+    // misc: TMEM base, abort flag, then the item ring ([2][3] ints: bh, row0, n)
+    static constexpr int kOffXMax = kOffMisc + 32;
     static constexpr int kOffXCarry = kOffXMax + 2 * 2 * 128 * 4;
     static constexpr int kOffXFin = kOffXCarry + 2 * 128 * 4;
     static constexpr int kSmemBytes = kOffXFin + 2 * 128 * 2 * 4 + 1024;  // + slack to align the base
@@ -122,10 +128,72 @@ struct TcParams {
     const __nv_bfloat16 *v0;
     __nv_bfloat16 *out;
     float *lse;
+    int num_items;  // query tiles: num_qtiles * B * H
+    int slot;       // this launch's scheduling counters
 };
+
+// A work item is one query tile of one (b, h).  Heads go in groups whose K/V
+// fit in L2 together; within a group the heaviest query tiles come first
+// (longest-first keeps the tail short).
+struct TcItem {
+    int bh, row0, n;  // n: key tiles (127-row stride) the query tile reads
+};
+
+__device__ __forceinline__ TcItem tc_item(int item, const TcParams &p) {
+    const int nq = p.num_qtiles, BH = p.B * p.H;
+    const int grp = item / (p.group * nq);
+    const int gsz = min(p.group, BH - grp * p.group);
+    const int idx = item - grp * p.group * nq;
+    TcItem w;
+    w.bh = grp * p.group + idx % gsz;
+    w.row0 = (nq - 1 - idx / gsz) * 128;
+    w.n = (min(w.row0 + 127, p.T - 1) + 1) / 127 + 1;
+    return w;
+}
+
+// Persistent scheduling: one CTA per SM; CTA b starts with item b and takes
+// the next one from a counter when it is about to need it.  Each launch draws
+// one of kSchedSlots counter pairs (round robin on the host), and the last CTA
+// of the launch to finish puts its pair back to zero, so launches that may run
+// at the same time (fewer than kSchedSlots apart) never share a counter.
+constexpr int kSchedSlots = 64;
+__device__ unsigned int g_sched_next[kSchedSlots];
+__device__ unsigned int g_sched_done[kSchedSlots];
 
 __device__ __forceinline__ bool wait_c(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
     return wait_bar(bar, parity, abort_flag, &g_tc_status);
+}
+
+// mbarrier.try_wait with a suspend-time hint (100 us): a thread whose phase is
+// not complete sleeps until it completes instead of polling.  Used where all
+// softmax warps wait on the tensor core at once (the end of an item), so that
+// their polling takes no issue slots from the MMA thread they wait for.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(100000u)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait, as wait_c, on the sleeping try_wait.
+__device__ __forceinline__ bool wait_s(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            *(volatile int *)&g_tc_status = kStatusTimeout;
+            __threadfence();
+            return false;
+        }
+    }
 }
 
 // ------------------------------------------------------------- weights
@@ -381,17 +449,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Heads go in groups whose K/V fit in L2 together; within a group the
-    // heaviest query tiles go first (longest-first keeps the tail short).
-    const int nq = p.num_qtiles, BH = p.B * p.H;
-    const int grp = (int)(blockIdx.x / (unsigned)(p.group * nq));
-    const int gsz = min(p.group, BH - grp * p.group);
-    const int idx = (int)blockIdx.x - grp * p.group * nq;
-    const int bh = grp * p.group + idx % gsz;
-    const int qtile = nq - 1 - idx / gsz;
     const int T = p.T;
-    const int row0 = qtile * 128;
-    const int n = (min(row0 + 127, T - 1) + 1) / 127 + 1;  // key tiles of this query tile
+    // the item ring: query tiles taken by the producer, decoded, read by every role
+    volatile int *item_ring = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 8);
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(C::kBarQ), 1);
@@ -409,6 +469,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(BAR(C::kBarODone), 1);
         mbar_init(BAR(C::kBarDrain), 1);
         mbar_init(BAR(C::kBarX), 256);
+        mbar_init(BAR(C::kBarQEmpty), 1);
+        mbar_init(BAR(C::kBarQRead), 4);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(BAR(C::kBarItemFull + s), 1);
+            mbar_init(BAR(C::kBarItemEmpty + s), 9);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -436,6 +502,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Item c of this CTA (c = 0, 1, ..) sits in ring slot c & 1; n = 0 marks the end.
+    auto take_item = [&](int c, TcItem &w) -> bool {
+        if (!wait_c(BAR(C::kBarItemFull + (c & 1)), (c >> 1) & 1, abort_flag)) return false;
+        const volatile int *e = item_ring + 3 * (c & 1);
+        w.bh = e[0];
+        w.row0 = e[1];
+        w.n = e[2];
+        return true;
+    };
+
     if (warp >= 8) {
       if (warp == kWarpProducer) {
         // ------------------------------------------------------ TMA producer
@@ -443,29 +519,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(BAR(C::kBarQ), C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_load_3d(sQ + c * kChunkBytes, &tm_q, 64 * c, row0, bh, BAR(C::kBarQ));
-            int issued_k = 0, issued_v = 0;
-            for (int j = 0; j < n; ++j) {
-                const int krow = 127 * j - 1;
-                const int sk = j % NSK;
-                if (!wait_c(BAR(C::kBarKEmpty + sk), ((j / NSK) & 1) ^ 1, abort_flag)) break;
-                mbar_arrive_expect_tx(BAR(C::kBarKFull + sk), C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sK + sk * C::kTileBytes + c * kChunkBytes, &tm_k, 64 * c, krow, bh,
-                                BAR(C::kBarKFull + sk));
-                issued_k = j + 1;
-                const int sv = j % NSV;
-                if (!wait_c(BAR(C::kBarVEmpty + sv), ((j / NSV) & 1) ^ 1, abort_flag)) break;
-                mbar_arrive_expect_tx(BAR(C::kBarVFull + sv), C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sV + sv * C::kVStageBytes + c * kChunkBytes, &tm_v, 64 * c, krow,
-                                bh, BAR(C::kBarVFull + sv));
-                issued_v = j + 1;
+            int item = (int)blockIdx.x;
+            int issued_q = 0, issued_k = 0, issued_v = 0;  // loads issued (K, V: tiles)
+            bool ok = true;
+            for (int c = 0; ok; ++c) {
+                ok = wait_c(BAR(C::kBarItemEmpty + (c & 1)), ((c >> 1) & 1) ^ 1, abort_flag);
+                if (!ok) break;
+                const bool last = item >= p.num_items;
+                TcItem w = {0, 0, 0};
+                if (!last) w = tc_item(item, p);
+                volatile int *e = item_ring + 3 * (c & 1);
+                e[0] = w.bh;
+                e[1] = w.row0;
+                e[2] = w.n;
+                mbar_arrive(BAR(C::kBarItemFull + (c & 1)));
+                if (last) break;
+                // Q is reloaded once the previous item's last S is done and,
+                // with a given sink, its rows' sink logits have been read from
+                // it (those reads follow the Q load they wait for, so QRead
+                // cannot run a phase ahead of this wait)
+                if (c > 0) {
+                    ok = wait_c(BAR(C::kBarQEmpty), (c - 1) & 1, abort_flag) &&
+                         (p.mode != 2 || wait_c(BAR(C::kBarQRead), (c - 1) & 1, abort_flag));
+                    if (!ok) break;
+                }
+                mbar_arrive_expect_tx(BAR(C::kBarQ), C::kTileBytes);
+                for (int cc = 0; cc < C::kChunks; ++cc)
+                    tma_load_3d(sQ + cc * kChunkBytes, &tm_q, 64 * cc, w.row0, w.bh, BAR(C::kBarQ));
+                issued_q = c + 1;
+                for (int j = 0; j < w.n; ++j) {
+                    const int krow = 127 * j - 1;
+                    const int g = issued_k;  // this CTA's key tile count
+                    const int sk = g % NSK;
+                    if (!(ok = wait_c(BAR(C::kBarKEmpty + sk), ((g / NSK) & 1) ^ 1, abort_flag))) break;
+                    mbar_arrive_expect_tx(BAR(C::kBarKFull + sk), C::kTileBytes);
+                    for (int cc = 0; cc < C::kChunks; ++cc)
+                        tma_load_3d(sK + sk * C::kTileBytes + cc * kChunkBytes, &tm_k, 64 * cc, krow,
+                                    w.bh, BAR(C::kBarKFull + sk));
+                    issued_k = g + 1;
+                    const int sv = g % NSV;
+                    if (!(ok = wait_c(BAR(C::kBarVEmpty + sv), ((g / NSV) & 1) ^ 1, abort_flag))) break;
+                    mbar_arrive_expect_tx(BAR(C::kBarVFull + sv), C::kTileBytes);
+                    for (int cc = 0; cc < C::kChunks; ++cc)
+                        tma_load_3d(sV + sv * C::kVStageBytes + cc * kChunkBytes, &tm_v, 64 * cc,
+                                    krow, w.bh, BAR(C::kBarVFull + sv));
+                    issued_v = g + 1;
+                }
+                // the next item, taken when this CTA is about to need it
+                item = (int)gridDim.x + (int)atomicAdd(&g_sched_next[p.slot], 1u);
             }
             // Let every copy this thread issued land before the block can exit.
-            wait_bar_drain(BAR(C::kBarQ), 0, &g_tc_status);
+            if (issued_q > 0) wait_bar_drain(BAR(C::kBarQ), (issued_q - 1) & 1, &g_tc_status);
             for (int j = max(0, issued_k - NSK); j < issued_k; ++j)
                 wait_bar_drain(BAR(C::kBarKFull + j % NSK), (j / NSK) & 1, &g_tc_status);
             for (int j = max(0, issued_v - NSV); j < issued_v; ++j)
@@ -477,48 +581,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdescS = make_idesc(128, 128, false);
             constexpr uint32_t kIdescO = make_idesc(128, C::kN, true);
-            bool ok = wait_c(BAR(C::kBarQ), 0, abort_flag);
-            tc_fence_after();
-            // S(j) = Q K_j^T into S buffer j % 2; K tile j is released once done
-            auto issue_s = [&](int j) -> bool {
-                if (!wait_c(BAR(C::kBarKFull + j % NSK), (j / NSK) & 1, abort_flag)) return false;
+            // One stream of key tiles over this CTA's items: within an item S
+            // runs two tiles ahead of PV; the next item's first S wait until
+            // this item's last PV is issued, since waiting for its Q must not
+            // hold that PV (and the epilogue) back.  So S and PV are always
+            // in the same item.
+            int c = -1, n = 0;    // the current item and its key tiles
+            int s_j = 0, p_j = 0;  // its S and PV issued
+            int gs = 0, gp = 0;    // S and PV issued over all items
+            // S(gs) = Q K^T into S buffer gs % 2; K tile gs is released once done
+            auto issue_s = [&]() -> bool {
+                if (!wait_c(BAR(C::kBarKFull + gs % NSK), (gs / NSK) & 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t kb = sK + (j % NSK) * C::kTileBytes;
+                const uint32_t kb = sK + (gs % NSK) * C::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    tc_mma_ss(tmem + C::col_s(j & 1), make_sdesc(sQ + off, 16, 1024),
+                    tc_mma_ss(tmem + C::col_s(gs & 1), make_sdesc(sQ + off, 16, 1024),
                               make_sdesc(kb + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(BAR(C::kBarSFull + (j & 1)));
-                tc_commit(BAR(C::kBarKEmpty + j % NSK));
+                tc_commit(BAR(C::kBarSFull + (gs & 1)));
+                tc_commit(BAR(C::kBarKEmpty + gs % NSK));
+                ++gs;
+                if (++s_j == n) tc_commit(BAR(C::kBarQEmpty));  // the item's last S
                 return true;
             };
-            // [O | rowsum] += P(j) [V_j | ones], P read from the TMEM of S buffer j % 2
-            auto issue_pv = [&](int j) -> bool {
-                if (!wait_c(BAR(C::kBarVFull + j % NSV), (j / NSV) & 1, abort_flag)) return false;
+            // the next item and its first two S (one if it has a single key
+            // tile); n = 0 once there is none
+            auto next_item = [&]() -> bool {
+                TcItem w;
+                if (!take_item(c + 1, w)) return false;
+                mbar_arrive(BAR(C::kBarItemEmpty + ((c + 1) & 1)));
+                ++c;
+                s_j = p_j = 0;
+                n = w.n;
+                if (n == 0) return true;
+                if (!wait_c(BAR(C::kBarQ), c & 1, abort_flag)) return false;
+                return issue_s() && (n == 1 || issue_s());
+            };
+            bool ok = next_item();
+            while (ok && n > 0) {
+                if (!(ok = wait_c(BAR(C::kBarPFull), gp & 1, abort_flag))) break;
                 tc_fence_after();
-                const uint32_t vb = sV + (j % NSV) * C::kVStageBytes;
+                // [O | rowsum] += P(gp) [V_gp | ones], P read from the TMEM of S buffer gp % 2
+                if (!(ok = wait_c(BAR(C::kBarVFull + gp % NSV), (gp / NSV) & 1, abort_flag))) break;
+                tc_fence_after();
+                const uint32_t vb = sV + (gp % NSV) * C::kVStageBytes;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_ts(tmem + C::kColO, tmem + C::col_s(j & 1) + p_col(kk >> 1) + (kk & 1) * 8,
+                    tc_mma_ts(tmem + C::kColO, tmem + C::col_s(gp & 1) + p_col(kk >> 1) + (kk & 1) * 8,
                               make_sdesc(vb + kk * 2048, kChunkBytes, 1024), kIdescO,
-                              (j > 0 || kk > 0) ? 1u : 0u);
+                              (p_j > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(BAR(C::kBarODone));
-                tc_commit(BAR(C::kBarVEmpty + j % NSV));
-                return true;
-            };
-            // S runs two tiles ahead of PV: while the softmax works on S(j+1),
-            // the tensor core computes PV(j) and S(j+2).
-            if (ok) ok = issue_s(0);
-            if (ok && n > 1) ok = issue_s(1);
-            for (int j = 0; ok && j < n; ++j) {
-                if (!(ok = wait_c(BAR(C::kBarPFull), j & 1, abort_flag))) break;
-                tc_fence_after();
-                if (!(ok = issue_pv(j))) break;
-                // S(j+2) overwrites the TMEM that PV(j) reads as P; both are
+                tc_commit(BAR(C::kBarVEmpty + gp % NSV));
+                ++gp;
+                ++p_j;
+                // S(gp+1) overwrites the TMEM that PV(gp-1) read as P; both are
                 // tcgen05.mma issued in order by this thread.
-                if (j + 2 < n && !(ok = issue_s(j + 2))) break;
+                if (s_j < n)
+                    ok = issue_s();
+                else if (p_j == n)
+                    ok = next_item();
             }
             // every MMA this thread issued completes before the block exits
             tc_commit(BAR(C::kBarDrain));
@@ -530,7 +653,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ softmax
         const int half = warp >> 2, wq = warp & 3;
         const int irow = wq * 32 + lane;
-        const int r = row0 + irow;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tO = tmem + lane_off + C::kColO;
         float *xmax = reinterpret_cast<float *>(smem + C::kOffXMax);
@@ -538,117 +660,131 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *xfin = reinterpret_cast<float *>(smem + C::kOffXFin);
         const uint32_t xbar = BAR(C::kBarX);
         uint32_t xe = 0;  // exchanges completed on xbar
-        RowState st;
-        st.k2 = p.k2;
-        st.m_run = -INFINITY;
-        st.l_run = st.w_sink = st.s_sink = 0.0f;
+        int g = 0;        // key tiles of this CTA done so far
         bool ok = true;
-        if (half == 0 && p.mode == 2) {
-            ok = __all_sync(0xffffffffu, wait_c(BAR(C::kBarQ), 0, abort_flag));
-            if (ok) {
-                // s_sink = q_r . k0[h], from this row of the swizzled Q tile
-                const __nv_bfloat16 *k0h = p.k0 + (size_t)(bh % p.H) * D;
-                float acc = 0.0f;
+        while (ok) {
+            // items done so far: one exchange per key tile, one more per item
+            const int c = (int)xe - g;
+            TcItem w;
+            ok = __all_sync(0xffffffffu, take_item(c, w));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(C::kBarItemEmpty + (c & 1)));
+            if (!ok || w.n == 0) break;
+            const int bh = w.bh, row0 = w.row0, n = w.n;
+            const int r = row0 + irow;
+            RowState st;
+            st.k2 = p.k2;
+            st.m_run = -INFINITY;
+            st.l_run = st.w_sink = st.s_sink = 0.0f;
+            if (half == 0) {
+                if (p.mode == 2) {
+                    ok = __all_sync(0xffffffffu, wait_c(BAR(C::kBarQ), c & 1, abort_flag));
+                    if (!ok) break;
+                    // s_sink = q_r . k0[h], from this row of the swizzled Q tile
+                    const __nv_bfloat16 *k0h = p.k0 + (size_t)(bh % p.H) * D;
+                    float acc = 0.0f;
 #pragma unroll
-                for (int cc = 0; cc < C::kChunks; ++cc) {
+                    for (int cc = 0; cc < C::kChunks; ++cc) {
 #pragma unroll
-                    for (int kc = 0; kc < 8; ++kc) {
-                        const uint8_t *src = smem + C::kOffQ + cc * kChunkBytes + irow * 128 +
-                                             ((kc ^ (irow & 7)) << 4);
-                        const uint4 qv = *reinterpret_cast<const uint4 *>(src);
-                        const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(&qv);
+                        for (int kc = 0; kc < 8; ++kc) {
+                            const uint8_t *src = smem + C::kOffQ + cc * kChunkBytes + irow * 128 +
+                                                 ((kc ^ (irow & 7)) << 4);
+                            const uint4 qv = *reinterpret_cast<const uint4 *>(src);
+                            const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(&qv);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            acc = fmaf(__bfloat162float(qb[e]),
-                                       __bfloat162float(k0h[cc * 64 + kc * 8 + e]), acc);
+                            for (int e = 0; e < 8; ++e)
+                                acc = fmaf(__bfloat162float(qb[e]),
+                                           __bfloat162float(k0h[cc * 64 + kc * 8 + e]), acc);
+                        }
                     }
+                    st.s_sink = acc;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(C::kBarQRead));
                 }
-                st.s_sink = acc;
             }
-        }
-        for (int j = 0; ok && j < n; ++j) {
-            const uint32_t tS = tmem + lane_off + C::col_s(j & 1);
-            ok = __all_sync(0xffffffffu,
-                            wait_c(BAR(C::kBarSFull + (j & 1)), (j >> 1) & 1, abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            // last valid column of this row, and whether the tile needs masks
-            const int c_last = r + 1 - 127 * j;
-            const bool masked = 127 * j + 127 > row0 + 1;
-            const int sink = j == 0 ? p.mode : 0;
-            // this half's 64 logits and its neighbour column (64 or 63)
-            uint32_t a[2][32];
-            uint32_t nb[1] = {0u};
-            tmem_ld32(tS + 64 * half, a[0]);
-            tmem_ld32(tS + 64 * half + 32, a[1]);
-            tmem_ld1(tS + (half == 0 ? 64 : 63), nb[0]);
-            tmem_wait_ld_regs<32>(a[0]);
-            tmem_wait_ld_regs<32>(a[1]);
-            tmem_wait_ld_regs<1>(nb);
-            float s0 = __uint_as_float(a[0][0]);
-            if (half == 0 && sink == 1) s0 = __uint_as_float(a[0][1]);
-            if (half == 0 && sink == 2) s0 = st.s_sink;
-            // the symmetric interval has no sink: its logit must not raise the max
-            if (SYM && half == 0 && j == 0) s0 = -INFINITY;
-            const float mine = masked ? half_max<true>(a, half, c_last, s0)
-                                      : half_max<false>(a, half, c_last, s0);
-            // exchange the partial maxima (and the carried L share) with the other half
-            const int slot = xe & 1;
-            xmax[(slot * 2 + half) * 128 + irow] = mine;
-            mbar_arrive(xbar);
-            ok = __all_sync(0xffffffffu, wait_c(xbar, xe & 1, abort_flag));
-            ++xe;
-            if (!ok) break;
-            const float mx = fmaxf(mine, xmax[(slot * 2 + (half ^ 1)) * 128 + irow]);
-            float Lc = 0.0f;
-            if (half == 0 && j > 0) Lc = xcarry[slot * 128 + irow];
-            const float mt = (!masked || c_last >= 0) ? mx * st.k2 : -INFINITY;
-            float alpha = 1.0f;
-            const bool grow = mt > st.m_run + 8.0f;
-            if (grow) {
-                alpha = ex2_approx(st.m_run - mt);
-                st.m_run = mt;
-                st.l_run *= alpha;
-                st.w_sink *= alpha;
-                if (!SHORT) Lc *= alpha;  // SHORT carries a raw logit
-            }
-            const float nm = -st.m_run;
-            if (masked)
-                half_weights<true, SHORT, SYM>(tS, a, nb[0], st, half, c_last, sink, j == 0, nm, Lc);
-            else
-                half_weights<false, SHORT, SYM>(tS, a, nb[0], st, half, c_last, sink, j == 0, nm, Lc);
-            if (half == 1) xcarry[(xe & 1) * 128 + irow] = Lc;
-            // Rescale O (this half's value columns; half 1 also the row-sum
-            // column) when the max moved, after PV(j-1) finished.
-            const bool need_o = grow && j > 0;
-            if (__any_sync(0xffffffffu, need_o)) {
-                ok = __all_sync(0xffffffffu, wait_c(BAR(C::kBarODone), (j - 1) & 1, abort_flag));
+            for (int j = 0; ok && j < n; ++j, ++g) {
+                const uint32_t tS = tmem + lane_off + C::col_s(g & 1);
+                ok = __all_sync(0xffffffffu,
+                                wait_c(BAR(C::kBarSFull + (g & 1)), (g >> 1) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
-                const float s = need_o ? alpha : 1.0f;
-#pragma unroll
-                for (int cc = 0; cc < D / 64; ++cc) {
-                    uint32_t o[32];
-                    const uint32_t ta = tO + half * (D / 2) + 32 * cc;
-                    tmem_ld32(ta, o);
-                    tmem_wait_ld_regs<32>(o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * s);
-                    tmem_st32(ta, o);
+                // last valid column of this row, and whether the tile needs masks
+                const int c_last = r + 1 - 127 * j;
+                const bool masked = 127 * j + 127 > row0 + 1;
+                const int sink = j == 0 ? p.mode : 0;
+                // this half's 64 logits and its neighbour column (64 or 63)
+                uint32_t a[2][32];
+                uint32_t nb[1] = {0u};
+                tmem_ld32(tS + 64 * half, a[0]);
+                tmem_ld32(tS + 64 * half + 32, a[1]);
+                tmem_ld1(tS + (half == 0 ? 64 : 63), nb[0]);
+                tmem_wait_ld_regs<32>(a[0]);
+                tmem_wait_ld_regs<32>(a[1]);
+                tmem_wait_ld_regs<1>(nb);
+                float s0 = __uint_as_float(a[0][0]);
+                if (half == 0 && sink == 1) s0 = __uint_as_float(a[0][1]);
+                if (half == 0 && sink == 2) s0 = st.s_sink;
+                // the symmetric interval has no sink: its logit must not raise the max
+                if (SYM && half == 0 && j == 0) s0 = -INFINITY;
+                const float mine = masked ? half_max<true>(a, half, c_last, s0)
+                                          : half_max<false>(a, half, c_last, s0);
+                // exchange the partial maxima (and the carried L share) with the other half
+                const int slot = xe & 1;
+                xmax[(slot * 2 + half) * 128 + irow] = mine;
+                mbar_arrive(xbar);
+                ok = __all_sync(0xffffffffu, wait_c(xbar, xe & 1, abort_flag));
+                ++xe;
+                if (!ok) break;
+                const float mx = fmaxf(mine, xmax[(slot * 2 + (half ^ 1)) * 128 + irow]);
+                float Lc = 0.0f;
+                if (half == 0 && j > 0) Lc = xcarry[slot * 128 + irow];
+                const float mt = (!masked || c_last >= 0) ? mx * st.k2 : -INFINITY;
+                float alpha = 1.0f;
+                const bool grow = mt > st.m_run + 8.0f;
+                if (grow) {
+                    alpha = ex2_approx(st.m_run - mt);
+                    st.m_run = mt;
+                    st.l_run *= alpha;
+                    st.w_sink *= alpha;
+                    if (!SHORT) Lc *= alpha;  // SHORT carries a raw logit
                 }
-                if (half == 1) {
-                    uint32_t o[1];
-                    tmem_ld1(tO + D, o[0]);
-                    tmem_wait_ld_regs<1>(o);
-                    o[0] = __float_as_uint(__uint_as_float(o[0]) * s);
-                    tmem_st1(tO + D, o[0]);
+                const float nm = -st.m_run;
+                if (masked)
+                    half_weights<true, SHORT, SYM>(tS, a, nb[0], st, half, c_last, sink, j == 0, nm, Lc);
+                else
+                    half_weights<false, SHORT, SYM>(tS, a, nb[0], st, half, c_last, sink, j == 0, nm, Lc);
+                if (half == 1) xcarry[(xe & 1) * 128 + irow] = Lc;
+                // Rescale O (this half's value columns; half 1 also the row-sum
+                // column) when the max moved, after PV of the previous tile finished.
+                const bool need_o = grow && j > 0;
+                if (__any_sync(0xffffffffu, need_o)) {
+                    ok = __all_sync(0xffffffffu, wait_c(BAR(C::kBarODone), (g - 1) & 1, abort_flag));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const float s = need_o ? alpha : 1.0f;
+#pragma unroll
+                    for (int cc = 0; cc < D / 64; ++cc) {
+                        uint32_t o[32];
+                        const uint32_t ta = tO + half * (D / 2) + 32 * cc;
+                        tmem_ld32(ta, o);
+                        tmem_wait_ld_regs<32>(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * s);
+                        tmem_st32(ta, o);
+                    }
+                    if (half == 1) {
+                        uint32_t o[1];
+                        tmem_ld1(tO + D, o[0]);
+                        tmem_wait_ld_regs<1>(o);
+                        o[0] = __float_as_uint(__uint_as_float(o[0]) * s);
+                        tmem_st1(tO + D, o[0]);
+                    }
+                    tmem_wait_st();
                 }
-                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(BAR(C::kBarPFull));
             }
-            tc_fence_before();
-            mbar_arrive(BAR(C::kBarPFull));
-        }
-        if (ok) {
+            if (!ok) break;
             // combine the two halves' fp32 sums; the given sink's weight lives in half 0
             float *mine = xfin + (half * 128 + irow) * 2;
             mine[0] = st.l_run;
@@ -656,50 +792,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(xbar);
             ok = __all_sync(0xffffffffu, wait_c(xbar, xe & 1, abort_flag));
             ++xe;
-        }
-        if (ok) {
+            if (!ok) break;
             const float *oth = xfin + ((half ^ 1) * 128 + irow) * 2;
             const float l_run = st.l_run + oth[0];
             const float w_sink = half == 0 ? st.w_sink : oth[1];
-            ok = __all_sync(0xffffffffu, wait_c(BAR(C::kBarODone), (n - 1) & 1, abort_flag));
-            if (ok) {
-                tc_fence_after();
-                // o is divided by the sum of exactly the bf16 weights that fed the
-                // PV product (O column d) plus the given sink's fp32 weight
-                uint32_t lb[1];
-                tmem_ld1(tO + D, lb[0]);
-                tmem_wait_ld_regs<1>(lb);
-                const float inv_l = 1.0f / (__uint_as_float(lb[0]) + w_sink);
-                const bool store = r < T;
-                __nv_bfloat16 *orow =
-                    p.out + ((size_t)bh * T + (size_t)(store ? r : 0)) * D + half * (D / 2);
-                const __nv_bfloat16 *v0h = p.v0 + (size_t)(bh % p.H) * D + half * (D / 2);
+            // O holds this item's last PV once it is done; the next item's
+            // first PV waits for this thread's PFull arrival, after the reads
+            ok = __all_sync(0xffffffffu, wait_s(BAR(C::kBarODone), (g - 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            // o is divided by the sum of exactly the bf16 weights that fed the
+            // PV product (O column d) plus the given sink's fp32 weight
+            uint32_t lb[1];
+            tmem_ld1(tO + D, lb[0]);
+            tmem_wait_ld_regs<1>(lb);
+            const float inv_l = 1.0f / (__uint_as_float(lb[0]) + w_sink);
+            const bool store = r < T;
+            __nv_bfloat16 *orow =
+                p.out + ((size_t)bh * T + (size_t)(store ? r : 0)) * D + half * (D / 2);
+            const __nv_bfloat16 *v0h = p.v0 + (size_t)(bh % p.H) * D + half * (D / 2);
 #pragma unroll
-                for (int cc = 0; cc < D / 64; ++cc) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + half * (D / 2) + 32 * cc, o);
-                    tmem_wait_ld_regs<32>(o);
-                    float val[32];
+            for (int cc = 0; cc < D / 64; ++cc) {
+                uint32_t o[32];
+                tmem_ld32(tO + half * (D / 2) + 32 * cc, o);
+                tmem_wait_ld_regs<32>(o);
+                float val[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float x = __uint_as_float(o[e]);
-                        if (p.mode == 2) x = fmaf(w_sink, __bfloat162float(v0h[32 * cc + e]), x);
-                        val[e] = x * inv_l;
-                    }
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(val[2 * e], val[2 * e + 1]);
-                    if (store) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * cc);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-                    }
+                for (int e = 0; e < 32; ++e) {
+                    float x = __uint_as_float(o[e]);
+                    if (p.mode == 2) x = fmaf(w_sink, __bfloat162float(v0h[32 * cc + e]), x);
+                    val[e] = x * inv_l;
                 }
-                if (store && half == 0 && p.lse)
-                    p.lse[(size_t)bh * T + r] =
-                        (st.m_run + log2f(l_run)) * kLn2 + (SHORT ? 0.0f : kLseShift);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(val[2 * e], val[2 * e + 1]);
+                if (store) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * cc);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                }
             }
+            if (store && half == 0 && p.lse)
+                p.lse[(size_t)bh * T + r] =
+                    (st.m_run + log2f(l_run)) * kLn2 + (SHORT ? 0.0f : kLseShift);
+            tc_fence_before();
         }
     }
 
@@ -707,6 +844,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+    // The last CTA to finish puts this launch's scheduling slot back to zero.
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&g_sched_done[p.slot], 1u) == gridDim.x - 1) {
+            atomicExch(&g_sched_next[p.slot], 0u);
+            atomicExch(&g_sched_done[p.slot], 0u);
+        }
+    }
 #undef BAR
 }
 
@@ -740,6 +885,44 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns) {
 }
 
 // ---------------------------------------------------------------- host side
+// Scheduling slots of one device.  A launch takes the next slot round robin;
+// the slot's event, recorded after its previous launch, orders the two, so a
+// slot's counters are reset before they are used again whatever streams the
+// launches run on.  (Stream capture skips the events: a captured graph keeps
+// its slot, and its replays follow one another on their stream.)
+struct SchedSlots {
+    std::mutex m;
+    unsigned next = 0;
+    cudaEvent_t ev[kSchedSlots] = {};
+};
+constexpr int kMaxDevices = 64;
+SchedSlots g_slots[kMaxDevices];
+
+template <class Launch>
+int launch_with_slot(int dev, cudaStream_t stream, Launch &&launch) {
+    if (dev < 0 || dev >= kMaxDevices) return CSA_ERR_UNSUPPORTED;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return CSA_ERR_CUDA;
+    SchedSlots &S = g_slots[dev];
+    std::lock_guard<std::mutex> lock(S.m);
+    const int slot = (int)(S.next++ % kSchedSlots);
+    cudaEvent_t &ev = S.ev[slot];
+    if (cap == cudaStreamCaptureStatusNone) {
+        if (ev == nullptr) {
+            if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+                ev = nullptr;
+                return CSA_ERR_CUDA;
+            }
+        } else if (cudaStreamWaitEvent(stream, ev, 0) != cudaSuccess) {
+            return CSA_ERR_CUDA;
+        }
+    }
+    if (!launch(slot)) return CSA_ERR_CUDA;
+    if (cap == cudaStreamCaptureStatusNone && cudaEventRecord(ev, stream) != cudaSuccess)
+        return CSA_ERR_CUDA;
+    return CSA_OK;
+}
+
 template <int D, bool SHORT, bool SYM>
 int launch_tc(const void *q, const void *k, const void *v, const void *k0, const void *v0,
               void *out, float *lse, int B, int H, int T, float scale, int mode,
@@ -762,14 +945,23 @@ int launch_tc(const void *q, const void *k, const void *v, const void *k0, const
     prm.v0 = static_cast<const __nv_bfloat16 *>(v0);
     prm.out = static_cast<__nv_bfloat16 *>(out);
     prm.lse = lse;
-    const long long grid = (long long)prm.num_qtiles * BH;
-    if (grid > 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
+    const long long items = (long long)prm.num_qtiles * BH;
+    if (items > 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
+    prm.num_items = (int)items;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return CSA_ERR_CUDA;
+    const unsigned grid = (unsigned)(items < sms ? items : sms);  // one CTA per SM
     auto kern = tc_forward_kernel<D, SHORT, SYM>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return CSA_ERR_CUDA;
-    kern<<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, prm);
-    return cudaGetLastError() == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+    return launch_with_slot(dev, stream, [&](int slot) {
+        prm.slot = slot;
+        kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, prm);
+        return cudaGetLastError() == cudaSuccess;
+    });
 }
 
 }  // namespace

@@ -26,6 +26,16 @@
  *  Memory     every pointer is DEVICE memory owned by the caller; the library
  *             allocates nothing and keeps no pointer after the call returns.
  *             out and lse must not overlap any input.
+ *  Scheduling the tensor-core forward kernels (csa_forward, its short-conv and
+ *             symmetric forms, and the kernels csa_forward_host launches)
+ *             run one CTA per SM and take query tiles from a counter in the
+ *             library's device image: 64 counter slots per device, drawn in
+ *             turn.  Each slot has one CUDA event, created on first use and
+ *             kept for the life of the process; a launch's stream waits on
+ *             its slot's event (the slot's previous launch), so calls on any
+ *             streams never share a counter.  Under stream capture the event
+ *             is left out: a captured graph keeps the slot it drew, and one
+ *             graph must not be replayed on two streams at the same time.
  *  Stream     the work is enqueued on `stream` (a cudaStream_t; NULL = the
  *             legacy default stream) and the call returns without waiting.
  *             Outputs are valid once the stream reaches that point.
