@@ -165,9 +165,10 @@ __device__ __forceinline__ bool wait_c(uint32_t bar, uint32_t parity, volatile i
 }
 
 // mbarrier.try_wait with a suspend-time hint (100 us): a thread whose phase is
-// not complete sleeps until it completes instead of polling.  Used where all
-// softmax warps wait on the tensor core at once (the end of an item), so that
-// their polling takes no issue slots from the MMA thread they wait for.
+// not complete sleeps until it completes instead of polling.  Used at the end
+// of an item, where all softmax warps wait while the MMA thread issues and
+// completes the item's last PV, so that their polling takes no issue slots
+// from it.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -790,7 +791,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mine[0] = st.l_run;
             mine[1] = st.w_sink;
             mbar_arrive(xbar);
-            ok = __all_sync(0xffffffffu, wait_c(xbar, xe & 1, abort_flag));
+            // sleeping: the MMA thread is issuing this item's last PV meanwhile
+            ok = __all_sync(0xffffffffu, wait_s(xbar, xe & 1, abort_flag));
             ++xe;
             if (!ok) break;
             const float *oth = xfin + ((half ^ 1) * 128 + irow) * 2;
@@ -811,11 +813,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             __nv_bfloat16 *orow =
                 p.out + ((size_t)bh * T + (size_t)(store ? r : 0)) * D + half * (D / 2);
             const __nv_bfloat16 *v0h = p.v0 + (size_t)(bh % p.H) * D + half * (D / 2);
+            uint32_t oc[D / 64][32];
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) tmem_ld32(tO + half * (D / 2) + 32 * cc, oc[cc]);
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) tmem_wait_ld_regs<32>(oc[cc]);
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
-                uint32_t o[32];
-                tmem_ld32(tO + half * (D / 2) + 32 * cc, o);
-                tmem_wait_ld_regs<32>(o);
+                const uint32_t *o = oc[cc];
                 float val[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
