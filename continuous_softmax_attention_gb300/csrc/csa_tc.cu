@@ -2,8 +2,13 @@
 // eq. (10)/(11) of Jianlin Su, "Continuous Softmax Attention" ("Assembly
 // and Simplification"), bf16 inputs, d = 64 or 128, fp32 accumulation.
 //
-// Work split.  One CTA owns one 128-row query tile of one (b, h) and walks
-// the key/value tiles up to its diagonal (heaviest query tiles launch first).
+// Work split.  A work item is one 128-row query tile of one (b, h); it walks
+// the key/value tiles up to its diagonal.  The grid is one persistent CTA per
+// SM: CTA b starts with item b and its producer warp takes further items from
+// a counter (heaviest query tiles first, heads grouped for L2), handing each
+// to the other warps through a two-entry ring.  The K/V rings, the S buffers
+// and O count over all of the CTA's key tiles and carry on from one item to
+// the next, so one item's epilogue overlaps the next item's first S products.
 // Warps:
 //   0-7  softmax: warp w owns rows 32*(w%4).. (its TMEM lane quarter) and,
 //        with w/4, the column half 0..63 or 64..127 of S
@@ -154,8 +159,9 @@ __device__ __forceinline__ TcItem tc_item(int item, const TcParams &p) {
 // Persistent scheduling: one CTA per SM; CTA b starts with item b and takes
 // the next one from a counter when it is about to need it.  Each launch draws
 // one of kSchedSlots counter pairs (round robin on the host), and the last CTA
-// of the launch to finish puts its pair back to zero, so launches that may run
-// at the same time (fewer than kSchedSlots apart) never share a counter.
+// of the launch to finish puts its pair back to zero.  The host orders each
+// launch after the slot's previous launch (an event per slot), so two
+// launches never use one counter at the same time.
 constexpr int kSchedSlots = 64;
 __device__ unsigned int g_sched_next[kSchedSlots];
 __device__ unsigned int g_sched_done[kSchedSlots];
