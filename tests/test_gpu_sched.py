@@ -69,3 +69,24 @@ def test_many_back_to_back_launches_one_stream():
     assert csa.device_status() == 0
     for o, lse in outs:
         assert torch.equal(o, ro) and torch.equal(lse, rl)
+
+
+@pytest.mark.parametrize("H, T", [(19, 1024), (17, 1152), (1, 19456), (3, 6400)])
+def test_item_counts_around_the_sm_count(H, T):
+    """Query tiles: 19 x 8 = 152 (one per CTA on a 152-SM part), 17 x 9 =
+    153 (one CTA takes a second), 152 in one head, 150 over three heads.
+    Every head of one launch is bit-identical to that head launched alone,
+    where each CTA holds at most one query tile."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    x = make_inputs(1, H, T, 128, "bf16", seed=7 + H)
+    g = {k: t.cuda() for k, t in x.items()}
+    scale = 128 ** -0.5
+    o, lse = csa.forward(g["q"], g["k"], g["v"], g["k0"], g["v0"], mode=2, scale=scale)
+    for h in range(H):
+        sl = lambda t: t[:, h:h + 1].contiguous()
+        oh, lh = csa.forward(sl(g["q"]), sl(g["k"]), sl(g["v"]), g["k0"][h:h + 1].contiguous(),
+                             g["v0"][h:h + 1].contiguous(), mode=2, scale=scale)
+        torch.cuda.synchronize()
+        assert torch.equal(o[:, h:h + 1], oh), (h, sms)
+        assert torch.equal(lse[:, h:h + 1], lh), (h, sms)
+    assert csa.device_status() == 0
