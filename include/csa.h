@@ -34,8 +34,10 @@
  *             kept for the life of the process; a launch's stream waits on
  *             its slot's event (the slot's previous launch), so calls on any
  *             streams never share a counter.  Under stream capture the event
- *             is left out: a captured graph keeps the slot it drew, and one
- *             graph must not be replayed on two streams at the same time.
+ *             is left out: a captured graph keeps the slot it drew, so a
+ *             replay must not run at the same time as another replay of the
+ *             same graph, nor as a later call that draws the same slot (every
+ *             64th forward call on the device).
  *  Stream     the work is enqueued on `stream` (a cudaStream_t; NULL = the
  *             legacy default stream) and the call returns without waiting.
  *             Outputs are valid once the stream reaches that point.
