@@ -46,12 +46,16 @@ def _worker(rank, world, port, B, H, T, d, mode, q):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("B,H,mode", [(2, 3, 2), (1, 5, 0), (3, 1, 1)])
-def test_two_gloo_ranks_match_single_process(B, H, mode):
+@pytest.mark.parametrize("B,H,mode,world", [(2, 3, 2, 2), (1, 5, 0, 2), (3, 1, 1, 2), (2, 3, 2, 4),
+                                            (1, 3, 0, 4)])
+def test_gloo_ranks_match_single_process(B, H, mode, world):
+    """world ranks each take a shard of the B*H problems (with 3 problems
+    over 4 ranks, one rank has none) and the gathered result equals one
+    process's."""
     import oracle
     from continuous_softmax_attention_gb300.inputs import make_inputs
 
-    T, d, world = 40, 8, 2
+    T, d = 40, 8
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
@@ -66,7 +70,7 @@ def test_two_gloo_ranks_match_single_process(B, H, mode):
     x = make_inputs(B, H, T, d, "f32", seed=42)
     ro, rl = oracle.forward(x["q"], x["k"], x["v"], x["k0"], x["v0"], scale=0.4, mode=mode)
     assert np.array_equal(o, ro) and np.array_equal(lse, rl)
-    assert t == 11.0
+    assert t == 10.0 + world - 1  # the max over ranks of 10 + rank
 
 
 def test_head_shard_partition():
