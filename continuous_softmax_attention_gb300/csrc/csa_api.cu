@@ -63,7 +63,6 @@ int forward_bf16(const void *q, const void *k, const void *v, const void *k0, co
     if ((rc = device_ok()) != CSA_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (d == 64 || d == 128) {
-        if (scale < 0.0f) return CSA_ERR_UNSUPPORTED;
         if (continuous)
             return csa_tc_forward(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, form, s);
         return csa_tc_std_forward(q, k, v, out, lse, B, H, T, d, scale, s);
@@ -251,7 +250,6 @@ int csa_forward_host_ex(const void *q, const void *k, const void *v, const void 
     if (need < 0 || workspace_bytes < need) return CSA_ERR_INVALID_ARG;
     if (!aligned(workspace, 256) || (lse && !aligned(lse, 4))) return CSA_ERR_ALIGNMENT;
     if (k0_mode == CSA_K0_GIVEN && (!aligned(k0, 2) || !aligned(v0, 2))) return CSA_ERR_ALIGNMENT;
-    if ((d == 64 || d == 128) && scale < 0.0f) return CSA_ERR_UNSUPPORTED;
     if ((rc = device_ok()) != CSA_OK) return rc;
     return csa_host_forward(q, k, v, k0, v0, out, lse, workspace, B, H, T, d, scale, k0_mode,
                             heads_per_chunk, !(flags & CSA_HOST_NO_ENTRY_WAIT),

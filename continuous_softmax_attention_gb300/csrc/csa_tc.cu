@@ -7,31 +7,36 @@
 // SM: CTA b starts with item b and its producer warp takes further items from
 // a counter (heaviest query tiles first, heads grouped for L2), handing each
 // to the other warps through a two-entry ring.  The K/V rings, the S buffers
-// and O count over all of the CTA's key tiles and carry on from one item to
-// the next, so one item's epilogue overlaps the next item's first S products.
-// Warps:
+// and the O accumulators count over all of the CTA's key tiles and carry on
+// from one item to the next, so one item's epilogue overlaps the next item's
+// first S products.  Warps:
 //   0-7  softmax: warp w owns rows 32*(w%4).. (its TMEM lane quarter) and,
-//        with w/4, the column half 0..63 or 64..127 of S
-//   8    TMA producer (lane 0; all lanes write the constant ones block once)
+//        with h = w/4, the half h of the key columns of each S tile
+//   8    TMA producer (lane 0; all lanes write the constant ones box once)
 //   9    TMEM allocator and tcgen05.mma issuer (lane 0)
-// Shared memory holds the Q tile, a K ring and a V ring of 128B-swizzled
-// 64-column boxes written by TMA.  Each V stage has one more box holding a
-// column of ones, so the PV product (N = d + 16) also accumulates, in O
-// column d, the row sum of exactly the bf16 P values it used.
-// Tensor memory (512 columns): S buffer 0 | S buffer 1 | O (d + 16 columns).
-// S is double-buffered: the tensor core computes PV(j) and S(j+2) while the
-// softmax works on S(j+1).  P (bf16) overwrites columns of its own S that
-// are no longer read (0..31 and 80..111) and is the A operand of the PV
-// product straight from TMEM.
+// Tensor memory (512 columns): S buffer 0 | S buffer 1 | O_0 | O_1.  S is
+// double-buffered: the tensor core computes PV(j) and S(j+2) while the
+// softmax works on S(j+1).  The two column halves are independent: each
+// has its own running max, its own fp32 row sum and its own accumulator O_h
+// (d + 16 columns), fed by its own PV product of 64 keys (P_h, bf16, over
+// the half's own S columns, zero where the 64 keys reach into the other
+// half).  They meet once per query tile, in the epilogue, where the two
+// partial results are scaled to a common max and added.  Each V stage
+// carries one more box holding a column of ones, so each PV product also
+// accumulates, in column d of O_h, the row sum of exactly the bf16 P values
+// it used.
 //
-// The halo for b.  b_{t,i} needs the logit of the key to the right of i.
-// Key tiles are loaded at a stride of 127 rows: an S tile covers 128
-// consecutive keys of the extended sequence (the sink first), its last
-// column is the first key of the next tile, and that column's P is 0.  Tile
-// j starts at array row 127*j - 1; for j = 0 this row is -1, which TMA fills
-// with zeros: the zero sink pair k_0 = v_0 = 0 comes for free, and the
-// copy-first and given modes only replace the first logit (and, for given
-// v_0, add w_0 * v_0 to the output at the end).
+// Key tiles and the halo.  b_{t,i} needs the logits of both neighbours of
+// key i.  An S tile has NK columns (112 at d = 128, so that two S buffers
+// and two accumulators fit; 128 at d = 64) and tiles start every NK - 2
+// keys: column 0 and column NK-1 are halos whose weights belong to the
+// neighbouring tiles, and every owned column 1..NK-2 has both neighbours in
+// the tile.  Column c of tile j is position e = (NK-2) j + c - 1 of the
+// extended sequence, whose position 0 is the sink pair and position i the
+// i-th key.  Tile j starts at array row (NK-2) j - 2; TMA fills the rows -2
+// and -1 with zeros, so the zero sink pair k_0 = v_0 = 0 is column 1 of tile
+// 0 at no cost; the copy-first and given modes replace its logit (and, for
+// given v_0, add w_0 * v_0 to the output at the end).
 //
 // The weights.  With the running max m (log2 units) and u = a*log2(e) - m,
 // p = 2^u, each interval between neighbouring keys contributes
@@ -41,21 +46,27 @@
 // follow from the interval integral S = (p_right - p_left)/x by
 // R = (S - p_left)/x and L = S - R, with a power series for small steps.
 // All weights carry a common factor (ln 2)^2, which cancels in o and is
-// removed from lse.
+// removed from lse.  The arithmetic runs on pairs of lanes (f32x2): in a
+// chunk of n keys, lane x takes key / interval i and lane y takes i + n/2.
+//
+// The running max of a half is the exact max of its columns in the query
+// tile's first key tile; it is not raised per tile.  Weights may then exceed
+// 1, which costs nothing in fp32 and bf16; a half-tile's bf16 P stays in
+// registers until the half-tile is done, and only when a chunk's weights sum
+// past 2^64 does the half take the exact max of its columns of the tile,
+// rescale O_h, and compute the half-tile again.
 //
 // The template flag SHORT turns the kernel into the short-conv reading of
-// eq. (13): b is replaced by its first-order term, so a key's weight is
-// 2^z with z an affine combination of its own and its neighbours' logits
+// eq. (13): b is replaced by its first-order term, so a key's weight is 2^z
+// with z an affine combination of its own and its neighbours' logits
 // (short_chunk) and no phi2 is formed.  SYM integrates over the symmetric
 // interval [1/2, t + 1/2] instead (constant half-cells at both ends, no
 // sink; cont_chunk).
 //
-// The two column halves of a row exchange their partial maxima, the L share
-// that crosses into the next tile, and their final sums through shared
-// memory, synchronised by an mbarrier.  Every mbarrier wait is bounded in
-// time; on expiry the kernel records CSA_ERR_TIMEOUT, every role skips its
-// remaining work, the MMA issuer waits for its own MMAs, the producer waits
-// for its own copies, and TMEM is freed.
+// Every mbarrier wait is bounded in time; on expiry the kernel records
+// CSA_ERR_TIMEOUT, every role skips its remaining work, the MMA issuer waits
+// for its own MMAs, the producer waits for its own copies, and TMEM is
+// freed.
 #include <mutex>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -63,6 +74,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "csa.h"
 #include "csa_internal.h"
@@ -79,19 +91,31 @@ constexpr int kWarpMma = 9;
 constexpr int kThreads = 32 * 10;
 // -log((ln 2)^2): removes the common weight factor from lse
 constexpr float kLseShift = 0.7330258411633287f;
+// |X| below this (log2 units) takes the small-step coefficients.
+constexpr float kTau = 0.0625f;
+// A half-cell p/2 of the symmetric interval, times the common (ln 2)^2.
+constexpr float kHalfCell = 0.5f * kLn2 * kLn2;
+// A chunk whose weights sum past this raises its half's running max.
+constexpr float kSumLimit = 18446744073709551616.0f;  // 2^64
 
 template <int D>
 struct TcCfg {
-    static constexpr int kChunks = D / 64;  // 64-column boxes per tile
-    static constexpr int kTileBytes = kChunks * kChunkBytes;
-    static constexpr int kVStageBytes = kTileBytes + kChunkBytes;  // values + ones box
-    static constexpr int kN = D + 16;                              // PV width
+    static constexpr int kNK = D == 128 ? 112 : 128;  // keys (columns) per S tile
+    static constexpr int kKS = kNK - 2;               // key-tile stride: owned columns
+    static constexpr int kH0 = kNK / 2;               // keys of each column half
+    static constexpr int kBoxes = D / 64;             // 64-column boxes per row
+    static constexpr int kQBox = 128 * 128;           // 128 rows x 128 bytes
+    static constexpr int kKBox = kNK * 128;           // NK rows x 128 bytes
+    static constexpr int kQBytes = kBoxes * kQBox;
+    static constexpr int kKBytes = kBoxes * kKBox;
+    static constexpr int kVBytes = (kBoxes + 1) * kKBox;  // values + ones box
+    static constexpr int kN = D + 16;                     // PV width
     static constexpr int kStagesK = D == 128 ? 2 : 3;
     static constexpr int kStagesV = D == 128 ? 2 : 3;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kTileBytes;
-    static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
-    static constexpr int kOffBar = kOffV + kStagesV * kVStageBytes;
+    static constexpr int kOffK = kOffQ + kQBytes;
+    static constexpr int kOffV = kOffK + kStagesK * kKBytes;
+    static constexpr int kOffBar = kOffV + kStagesV * kVBytes;
     // barrier indices
     static constexpr int kBarQ = 0;
     static constexpr int kBarKFull = 1;
@@ -99,35 +123,37 @@ struct TcCfg {
     static constexpr int kBarVFull = kBarKEmpty + kStagesK;
     static constexpr int kBarVEmpty = kBarVFull + kStagesV;
     static constexpr int kBarSFull = kBarVEmpty + kStagesV;  // [2] one per S buffer
+    // [2 halves][2 S buffers]: a half may run up to two tiles ahead of the
+    // other, so each half's arrivals alternate between two barriers (one
+    // phase per two tiles) and none completes twice before it is consumed
     static constexpr int kBarPFull = kBarSFull + 2;
-    static constexpr int kBarODone = kBarPFull + 1;
+    static constexpr int kBarODone = kBarPFull + 4;
     static constexpr int kBarDrain = kBarODone + 1;
-    static constexpr int kBarX = kBarDrain + 1;  // half-to-half exchange
-    static constexpr int kBarQEmpty = kBarX + 1;     // an item's last S is done
+    static constexpr int kBarX = kBarDrain + 1;       // half-to-half exchange (epilogue)
+    static constexpr int kBarQEmpty = kBarX + 1;      // an item's last S is done
     static constexpr int kBarQRead = kBarQEmpty + 1;  // its sink logits are read from Q
-    static constexpr int kBarItemFull = kBarQRead + 1;    // [2] item ring
+    static constexpr int kBarItemFull = kBarQRead + 1;      // [2] item ring
     static constexpr int kBarItemEmpty = kBarItemFull + 2;  // [2]
     static constexpr int kNumBars = kBarItemEmpty + 2;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    // exchange buffers between the two column halves of the query tile:
-    //   xmax   [2 slots][2 halves][128 rows]  partial row maxima
-    //   xcarry [2 slots][128 rows]            L share carried to the next tile
-    //   xfin   [2 halves][128 rows][2]        final fp32 sum, sink weight
     // misc: TMEM base, abort flag, then the item ring ([2][3] ints: bh, row0, n)
-    static constexpr int kOffXMax = kOffMisc + 32;
-    static constexpr int kOffXCarry = kOffXMax + 2 * 2 * 128 * 4;
-    static constexpr int kOffXFin = kOffXCarry + 2 * 128 * 4;
-    static constexpr int kSmemBytes = kOffXFin + 2 * 128 * 2 * 4 + 1024;  // + slack to align the base
-    // TMEM columns: S buffer 0 | S buffer 1 | O
-    __device__ static constexpr uint32_t col_s(int b) { return 128u * (uint32_t)b; }
-    static constexpr uint32_t kColO = 256u;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    // the epilogue's exchange: [2 halves][128 rows][4] (max, sum, sink weight)
+    static constexpr int kOffXFin = kOffMisc + 64;
+    static constexpr int kSmemBytes = kOffXFin + 2 * 128 * 4 * 4 + 1024;  // + slack to align the base
+    // TMEM columns: S buffer 0 | S buffer 1 | O_0 | O_1
+    __device__ static constexpr uint32_t col_s(int b) { return (uint32_t)(kNK * b); }
+    __device__ static constexpr uint32_t col_o(int h) { return (uint32_t)(2 * kNK + kN * h); }
+    // P of half h: 64 keys (32 packed columns) over the half's own S columns
+    __device__ static constexpr uint32_t col_p(int h) { return h ? (uint32_t)(kNK - 32) : 0u; }
+    static_assert(2 * kNK + 2 * kN <= 512, "TMEM budget");
+    static_assert(kH0 == 56 || kH0 == 64, "column halves of 56 or 64 keys");
 };
 
 struct TcParams {
     int B, H, T;
     int num_qtiles;
     int group;  // heads per scheduling group
-    float k2;  // scale * log2(e)
+    float k2;   // scale * log2(e)
     int mode;
     const __nv_bfloat16 *k0;
     const __nv_bfloat16 *v0;
@@ -141,9 +167,10 @@ struct TcParams {
 // fit in L2 together; within a group the heaviest query tiles come first
 // (longest-first keeps the tail short).
 struct TcItem {
-    int bh, row0, n;  // n: key tiles (127-row stride) the query tile reads
+    int bh, row0, n;  // n: key tiles the query tile reads
 };
 
+template <int KS>
 __device__ __forceinline__ TcItem tc_item(int item, const TcParams &p) {
     const int nq = p.num_qtiles, BH = p.B * p.H;
     const int grp = item / (p.group * nq);
@@ -152,7 +179,7 @@ __device__ __forceinline__ TcItem tc_item(int item, const TcParams &p) {
     TcItem w;
     w.bh = grp * p.group + idx % gsz;
     w.row0 = (nq - 1 - idx / gsz) * 128;
-    w.n = (min(w.row0 + 127, p.T - 1) + 1) / 127 + 1;
+    w.n = (min(w.row0 + 127, p.T - 1) + 1) / KS + 1;
     return w;
 }
 
@@ -171,10 +198,7 @@ __device__ __forceinline__ bool wait_c(uint32_t bar, uint32_t parity, volatile i
 }
 
 // mbarrier.try_wait with a suspend-time hint (100 us): a thread whose phase is
-// not complete sleeps until it completes instead of polling.  Used at the end
-// of an item, where all softmax warps wait while the MMA thread issues and
-// completes the item's last PV, so that their polling takes no issue slots
-// from it.
+// not complete sleeps until it completes instead of polling.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -203,10 +227,67 @@ __device__ __forceinline__ bool wait_s(uint32_t bar, uint32_t parity, volatile i
     }
 }
 
-// ------------------------------------------------------------- weights
-// |X| below this (log2 units) takes the small-step coefficients.
-constexpr float kTau = 0.0625f;
+// ------------------------------------------------------------- TMEM access
+// 32 lanes x 16 (8) consecutive 32-bit columns: thread i gets lane (base+i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        : "memory");
+}
+// tcgen05.wait::ld naming the destination registers of the loads it waits
+// for, so that no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld8(uint32_t (&r)[8]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7])
+                 :
+                 : "memory");
+}
 
+// K and V viewed as csa_tc_common's 3-D tensor {D, T, B*H}, with boxes of
+// 64 columns x `rows` rows (the key-tile height).
+inline bool encode_rows_map(CUtensorMap *map, const void *ptr, int BH, int T, int D, int rows) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult rc = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return rc == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------- weights
 // One interval's two end weights, times (ln 2)^2.  X = u_right - u_left in
 // log2 units, p = 2^u, x = X ln2 the logit step.
 // Closed form (|X| >= 1/16):
@@ -218,6 +299,8 @@ constexpr float kTau = 0.0625f;
 //     sig = (p0 + p1) ln2/2,  R = (ln2)^2 (2 p0 + p1)/6,  L = (ln2)^2 (p0 + 2 p1)/6,
 // which match p0 phi2(x) and p1 phi2(-x) to (x^2)/12 relative (< 1.6e-4).
 // Both errors are below the 2^-9 rounding of the bf16 P these weights become.
+// The kernel runs seg_weights2, the same operations on two intervals at
+// once; this scalar form serves the test hook.
 __device__ __forceinline__ void seg_weights(float X, float p0, float p1, float &R, float &L) {
     const float rx = rcp_approx(X);
     const bool small = fabsf(X) < kTau;
@@ -230,61 +313,123 @@ __device__ __forceinline__ void seg_weights(float X, float p0, float p1, float &
     L = fmaf(sig, kLn2, -R);
 }
 
-// One 32-column chunk of weights.  sv[0..32] are the raw logits q.k of
-// columns cbase..cbase+32; Lc is the L share of column cbase coming from the
-// left.  Produces w[0..31] (e^{a+b-m} * (ln2)^2), returns in Lc the L share
-// of column cbase+32, and in L31 that of cbase+31.
-// SYM, the symmetric interval [1/2, t + 1/2] with constant end half-cells:
-// with first_cell (the chunk holding the sink and key 1) the sink takes no
-// weight and key 1's left share is its half-cell p_1/2; each row's last key
-// (MASKED) adds its right half-cell p/2 (both times (ln 2)^2).
-template <bool MASKED, bool SYM>
-__device__ __forceinline__ void cont_chunk(const float (&sv)[33], float k2, float nm, int cbase,
-                                           int c_last, bool first_cell, float &Lc, float &L31,
-                                           float (&w)[32]) {
-    constexpr float kHalfCell = 0.5f * kLn2 * kLn2;
-    float u[33], pe[33], L[33], R[32];
+// Two intervals (lanes x and y).  R: the left keys' shares; Ln: minus the
+// right keys' shares (R - sig ln2, the same rounding as -L above).
+__device__ __forceinline__ void seg_weights2(float2 X, float2 p0, float2 p1, float2 &R,
+                                             float2 &Ln) {
+    const float rxx = rcp_approx(X.x), rxy = rcp_approx(X.y);
+    const bool sx = fabsf(X.x) < kTau, sy = fabsf(X.y) < kTau;
+    const float2 a1 = make_float2(sx ? 1.0f : -1.0f, sy ? 1.0f : -1.0f);
+    const float2 f1 = make_float2(sx ? 0.5f * kLn2 : rxx, sy ? 0.5f * kLn2 : rxy);
+    const float2 f2 = make_float2(sx ? kLn2 / 3.0f : rxx, sy ? kLn2 / 3.0f : rxy);
+    const float2 a2 = __ffma2_rn(a1, make_float2(0.75f * kLn2, 0.75f * kLn2),
+                                 make_float2(-0.25f * kLn2, -0.25f * kLn2));
+    const float2 sig = __fmul2_rn(__ffma2_rn(p0, a1, p1), f1);
+    R = __fmul2_rn(__ffma2_rn(p0, a2, sig), f2);
+    Ln = __ffma2_rn(sig, make_float2(-kLn2, -kLn2), R);
+}
+
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
+// Per-row state of one softmax thread (one column half of one row).
+struct RowState {
+    float k2;      // scale * log2(e)
+    float m;       // this half's running max of the logits, log2 units
+    float l;       // fp32 sum of this half's weights (gives lse)
+    float w_sink;  // weight of the given sink pair (k0, v0 supplied), half 0
+    float s_sink;  // q . k0 of the given sink pair
+    int mode;      // sink mode
+};
+
+// The weights of a chunk of NCK keys (16 or 8) of one half-row: the keys of
+// columns cb..cb+NCK-1.  s[0..NCK]: their raw logits q.k and that of column
+// cb+NCK.  Lnc: minus the L share key cb receives from interval (cb-1, cb);
+// on return that of column cb+NCK.  EDGE_L / EDGE_R: the chunk is the first
+// / last of its half, so that its first key may be the tile's left halo
+// (halo_l), or the sink (sink: column 1 of the query tile's first key tile),
+// and its last key the right halo (halo_r).  SYM: the symmetric interval
+// [1/2, t + 1/2] with constant end half-cells: in the first tile the sink
+// takes no weight and key 1's left share is its half-cell p_1/2; each row's
+// last key (MASKED) adds its right half-cell p/2 (both times (ln 2)^2).
+// Produces the bf16 P (pk, keys paired in order) and the keys' fp32 sum
+// (csum); w1 is the weight of column cb+1 (the sink's, when sink).
+template <int NCK, bool MASKED, bool SYM, bool EDGE_L, bool EDGE_R>
+__device__ __forceinline__ void cont_chunk(const float (&s)[NCK + 1], const RowState &st, float nm,
+                                           int cb, int c_last, bool halo_l, bool sink,
+                                           bool halo_r, float &Lnc, uint32_t (&pk)[NCK / 2],
+                                           float2 &csum, float &w1) {
+    constexpr int NH = NCK / 2;
+    float u[NCK + 1], p[NCK + 1];
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-        const float2 t = __ffma2_rn(make_float2(sv[i], sv[i + 1]), make_float2(k2, k2),
-                                    make_float2(nm, nm));
-        u[i] = t.x;
-        u[i + 1] = t.y;
+    for (int i = 0; i <= NCK; ++i) {
+        float sv = s[i];
+        if (EDGE_L && !SYM && i == 1) {
+            // the sink's logit: k_0 = k_1 (copy-first) or the given q.k0
+            const float alt = st.mode == CSA_K0_GIVEN ? st.s_sink : s[2];
+            sv = sink && st.mode != CSA_K0_ZERO ? alt : sv;
+        }
+        u[i] = fmaf(sv, st.k2, nm);
+        p[i] = ex2_approx(u[i]);
     }
-    u[32] = fmaf(sv[32], k2, nm);
+    float2 R[NH], Ln[NH];
 #pragma unroll
-    for (int i = 0; i < 33; ++i) pe[i] = ex2_approx(u[i]);
-    L[0] = Lc;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        float Ri, Li;
-        seg_weights(u[i + 1] - u[i], pe[i], pe[i + 1], Ri, Li);
+    for (int k = 0; k < NH; ++k) {
+        const float2 X = __ffma2_rn(make_float2(u[k], u[k + NH]), make_float2(-1.0f, -1.0f),
+                                    make_float2(u[k + 1], u[k + NH + 1]));
+        seg_weights2(X, make_float2(p[k], p[k + NH]), make_float2(p[k + 1], p[k + NH + 1]), R[k],
+                     Ln[k]);
         if (MASKED) {
             // interval (c, c+1) exists for this row only if c+1 <= its last key
-            const bool seg_ok = cbase + i + 1 <= c_last;
-            Ri = seg_ok ? Ri : 0.0f;
-            Li = seg_ok ? Li : 0.0f;
+            const bool vx = cb + k + 1 <= c_last, vy = cb + k + NH + 1 <= c_last;
+            R[k] = make_float2(vx ? R[k].x : 0.0f, vy ? R[k].y : 0.0f);
+            Ln[k] = make_float2(vx ? Ln[k].x : 0.0f, vy ? Ln[k].y : 0.0f);
         }
-        if (SYM && i == 0 && first_cell) {
-            Ri = 0.0f;                    // the sink is not part of [1/2, t + 1/2]
-            Li = kHalfCell * pe[1];       // key 1's left half-cell
-        }
-        R[i] = Ri;
-        L[i + 1] = Li;
     }
+    if (EDGE_L) {
+        // column 0 of the first tile is no position: no interval (0, 1)
+        Ln[0].x = sink ? 0.0f : Ln[0].x;
+        if (SYM) {
+            R[1].x = sink ? 0.0f : R[1].x;
+            Ln[1].x = sink ? -kHalfCell * p[2] : Ln[1].x;
+        }
+    }
+    float2 W[NH];
+    W[0] = __ffma2_rn(make_float2(Lnc, Ln[NH - 1].x), make_float2(-1.0f, -1.0f), R[0]);
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-        const float2 t = __fadd2_rn(make_float2(L[i], L[i + 1]), make_float2(R[i], R[i + 1]));
-        w[i] = t.x;
-        w[i + 1] = t.y;
-    }
+    for (int k = 1; k < NH; ++k) W[k] = __ffma2_rn(Ln[k - 1], make_float2(-1.0f, -1.0f), R[k]);
+    Lnc = Ln[NH - 1].y;
     if (SYM && MASKED) {
+        // each row's last key adds its right half-cell p/2
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            w[i] = cbase + i == c_last ? fmaf(kHalfCell, pe[i], w[i]) : w[i];  // right half-cell
+        for (int k = 0; k < NH; ++k) {
+            W[k].x = cb + k == c_last ? fmaf(kHalfCell, p[k], W[k].x) : W[k].x;
+            W[k].y = cb + k + NH == c_last ? fmaf(kHalfCell, p[k + NH], W[k].y) : W[k].y;
+        }
     }
-    L31 = L[31];
-    Lc = L[32];
+    if (EDGE_L) W[0].x = halo_l ? 0.0f : W[0].x;
+    if (EDGE_R) W[NH - 1].y = halo_r ? 0.0f : W[NH - 1].y;
+    w1 = W[1].x;
+    if (EDGE_L && !SYM) {
+        // v_0 = v_1: the sink's weight lands on key 1; a given v_0's share
+        // w_0 v_0 is added in fp32 at the end
+        const bool copy = sink && st.mode == CSA_K0_COPY_FIRST;
+        const bool given = sink && st.mode == CSA_K0_GIVEN;
+        W[2].x = copy ? W[2].x + W[1].x : W[2].x;
+        W[1].x = copy || given ? 0.0f : W[1].x;
+    }
+    float2 t = W[0];
+#pragma unroll
+    for (int k = 1; k < NH; ++k) t = __fadd2_rn(t, W[k]);
+    csum = t;
+#pragma unroll
+    for (int m = 0; m < NH / 2; ++m) {
+        pk[m] = pack_bf16x2(W[2 * m].x, W[2 * m + 1].x);
+        pk[NH / 2 + m] = pack_bf16x2(W[2 * m].y, W[2 * m + 1].y);
+    }
 }
 
 // The short-conv reading of eq. (13): a key's weight is 2^z, with z in log2
@@ -293,149 +438,274 @@ __device__ __forceinline__ void cont_chunk(const float (&sv)[33], float k2, floa
 //   one-sided ends   z = (2 u_c + u_nb) / 3 - 1   (the sink; each row's last key)
 // (-1 is log2 of the 1/2 in log phi2(x) = -log 2 + x/3 + ...).  Every z is a
 // convex combination of logits minus a constant, so the running max of the
-// raw logits still bounds it.  sv[0..32] are the raw logits of columns
-// cbase..cbase+32, sl that of column cbase-1 (unused when first_end: the
-// sink).  Produces w[0..31].
-template <bool MASKED>
-__device__ __forceinline__ void short_chunk(const float (&sv)[33], float sl, float k2, float nm,
-                                            int cbase, int c_last, bool first_end,
-                                            float (&w)[32]) {
+// raw logits still bounds it.  Arguments as cont_chunk; ul is the u of
+// column cb-1 on entry and that of column cb+NCK-1 on return.
+template <int NCK, bool MASKED, bool EDGE_L, bool EDGE_R>
+__device__ __forceinline__ void short_chunk(const float (&s)[NCK + 1], const RowState &st, float nm,
+                                            int cb, int c_last, bool halo_l, bool sink,
+                                            bool halo_r, float &ul, uint32_t (&pk)[NCK / 2],
+                                            float2 &csum, float &w1) {
+    constexpr int NH = NCK / 2;
     constexpr float kThird = 1.0f / 3.0f, kSixth = 1.0f / 6.0f;
-    float u[34];
-    u[0] = fmaf(sl, k2, nm);
+    float u[NCK + 2];  // u[i + 1] is column cb + i
+    u[0] = ul;
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-        const float2 t = __ffma2_rn(make_float2(sv[i], sv[i + 1]), make_float2(k2, k2),
-                                    make_float2(nm, nm));
-        u[i + 1] = t.x;
-        u[i + 2] = t.y;
-    }
-    u[33] = fmaf(sv[32], k2, nm);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const float ul = u[i], uc = u[i + 1], ur = u[i + 2];
-        float z = fmaf(ul + ur, kSixth, 4.0f * kSixth * uc);
-        if (i == 0 && first_end) z = fmaf(ur, kThird, fmaf(2.0f * kThird, uc, -1.0f));
-        if (MASKED) {
-            const int c = cbase + i;
-            const float zl = fmaf(ul, kThird, fmaf(2.0f * kThird, uc, -1.0f));
-            z = c == c_last ? zl : z;
-            w[i] = c <= c_last ? ex2_approx(z) : 0.0f;
-        } else {
-            w[i] = ex2_approx(z);
+    for (int i = 0; i <= NCK; ++i) {
+        float sv = s[i];
+        if (EDGE_L && i == 1) {
+            const float alt = st.mode == CSA_K0_GIVEN ? st.s_sink : s[2];
+            sv = sink && st.mode != CSA_K0_ZERO ? alt : sv;
         }
+        u[i + 1] = fmaf(sv, st.k2, nm);
+    }
+    ul = u[NCK];
+    float2 W[NH];
+#pragma unroll
+    for (int k = 0; k < NH; ++k) {
+        const float2 uc = make_float2(u[k + 1], u[k + NH + 1]);
+        const float2 nbs =
+            __fadd2_rn(make_float2(u[k], u[k + NH]), make_float2(u[k + 2], u[k + NH + 2]));
+        const float2 z = __ffma2_rn(nbs, make_float2(kSixth, kSixth),
+                                    __fmul2_rn(uc, make_float2(4.0f * kSixth, 4.0f * kSixth)));
+        float zz[2] = {z.x, z.y};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int i = k + NH * hh;  // key cb + i
+            if (EDGE_L && i == 1) {
+                // the sink is a one-sided end (right neighbour only)
+                zz[hh] = sink ? fmaf(u[i + 2], kThird, fmaf(2.0f * kThird, u[i + 1], -1.0f)) : zz[hh];
+            }
+            if (MASKED) {
+                const int c = cb + i;
+                const float zl = fmaf(u[i], kThird, fmaf(2.0f * kThird, u[i + 1], -1.0f));
+                zz[hh] = c == c_last ? zl : zz[hh];
+                zz[hh] = c <= c_last ? ex2_approx(zz[hh]) : 0.0f;
+            } else {
+                zz[hh] = ex2_approx(zz[hh]);
+            }
+        }
+        W[k] = make_float2(zz[0], zz[1]);
+    }
+    if (EDGE_L) W[0].x = halo_l ? 0.0f : W[0].x;
+    if (EDGE_R) W[NH - 1].y = halo_r ? 0.0f : W[NH - 1].y;
+    w1 = W[1].x;
+    if (EDGE_L) {
+        const bool copy = sink && st.mode == CSA_K0_COPY_FIRST;
+        const bool given = sink && st.mode == CSA_K0_GIVEN;
+        W[2].x = copy ? W[2].x + W[1].x : W[2].x;
+        W[1].x = copy || given ? 0.0f : W[1].x;
+    }
+    float2 t = W[0];
+#pragma unroll
+    for (int k = 1; k < NH; ++k) t = __fadd2_rn(t, W[k]);
+    csum = t;
+#pragma unroll
+    for (int m = 0; m < NH / 2; ++m) {
+        pk[m] = pack_bf16x2(W[2 * m].x, W[2 * m + 1].x);
+        pk[NH / 2 + m] = pack_bf16x2(W[2 * m].y, W[2 * m + 1].y);
     }
 }
 
-// Per-row online-softmax state of one softmax thread.
-struct RowState {
-    float k2;      // scale * log2(e)
-    float m_run;   // running max of the logits, log2 units
-    float l_run;   // fp32 sum of this half's weights (gives lse)
-    float w_sink;  // weight of the given sink pair (k0, v0 supplied)
-    float s_sink;  // q . k0 of the given sink pair
-};
-
-// Pass 1 of a half tile: max of the raw logits over this warp's 64 columns
-// (valid columns only; column 0 replaced by the sink logit if any).
-template <bool MASKED>
-__device__ __forceinline__ float half_max(const uint32_t (&a)[2][32], int half, int c_last,
-                                          float s0) {
-    float m[4];
+// Max of the valid scaled logits a*log2(e) of one half-row in the query
+// tile's first key tile: the half's columns and the neighbour column its
+// intervals reach (columns c0..c0+h0, c0 = h (h0 - 1)).  Column 0 is no
+// position there, column 1 is the sink (none in SYM).  -inf if the half
+// holds none of the row's keys; it then holds none of them in any later
+// tile either.
+template <bool SYM>
+__device__ __forceinline__ float first_tile_max(uint32_t tS, const RowState &st, int c0, int h0,
+                                                int c_last) {
+    float m = -INFINITY;
+#pragma unroll 1
+    for (int o = 0; o <= h0; o += 8) {
+        uint32_t t[8];
+        tmem_ld8(tS + c0 + o, t);
+        tmem_wait_ld8(t);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) m[i] = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 64; c += 2) {
-        const int col = 64 * half + c;
-        float v0 = c == 0 ? s0 : __uint_as_float(a[c >> 5][c & 31]);
-        float v1 = __uint_as_float(a[(c + 1) >> 5][(c + 1) & 31]);
-        if (MASKED) {
-            v0 = col <= c_last ? v0 : -INFINITY;
-            v1 = col + 1 <= c_last ? v1 : -INFINITY;
+        for (int i = 0; i < 8; ++i) {
+            const int col = c0 + o + i;
+            float v = __uint_as_float(t[i]);
+            if (col == 1 && st.mode == CSA_K0_GIVEN) v = st.s_sink;
+            // the copied sink duplicates column 2
+            const bool skip = col == 0 || (col == 1 && (SYM || st.mode == CSA_K0_COPY_FIRST)) ||
+                              o + i > h0;
+            m = !skip && col <= c_last ? fmaxf(m, v * st.k2) : m;
         }
-        m[(c >> 1) & 3] = fmax3f(m[(c >> 1) & 3], v0, v1);
     }
-    return fmax3f(m[0], m[1], fmaxf(m[2], m[3]));
+    return m;
 }
 
-// TMEM column where the P of 32 keys of S (16 packed columns) is written:
-// half 0's keys 0..63 go to columns 0..31 of S, half 1's keys 64..127 to
-// 80..111: columns that by then only their own warp has read.
-__device__ __forceinline__ uint32_t p_col(int k) { return k < 2 ? 16u * k : 80u + 16u * (k - 2); }
-
-// Pass 2 of a half tile: weights of this warp's 64 keys, P written to TMEM,
-// fp32 sum accumulated.  a: the half's 64 logits; nb: column 64 for half 0
-// (right neighbour of its last key), column 63 for half 1 (left neighbour
-// of its first key).  Lc enters as the L share of the half's first key
-// coming from the left and leaves (half 1) as that of the halo key, the
-// next tile's first key.
-// SHORT: the short-conv reading of eq. (13) (short_chunk); Lc then carries
-// raw logits instead of L shares: in, the logit of the column left of the
-// half's first key (for half 0 of the first tile: none, the sink is an end);
-// out (half 1), that of column 126, the left neighbour of the next tile's
-// first key.  tile0: this is the first key tile (column 0 is the sink).
-template <bool MASKED, bool SHORT, bool SYM>
-__device__ __forceinline__ void half_weights(uint32_t tS, const uint32_t (&a)[2][32], uint32_t nb,
-                                             RowState &st, int half, int c_last, int sink,
-                                             bool tile0, float nm, float &Lc) {
-    const float k2 = st.k2;
-    if (SHORT && half == 1) Lc = __uint_as_float(nb);  // column 63
-    if (!SHORT && half == 1) {
-        // interval (63, 64) gives key 64 its share from the left
-        const float u0 = fmaf(__uint_as_float(nb), k2, nm);
-        const float u1 = fmaf(__uint_as_float(a[0][0]), k2, nm);
-        float R, L;
-        seg_weights(u1 - u0, ex2_approx(u0), ex2_approx(u1), R, L);
-        Lc = (!MASKED || 64 <= c_last) ? L : 0.0f;
+// Raises a half's running max when a chunk's weights came out too large (the
+// whole warp calls it; lanes whose max does not move scale by 1).  The new
+// max is the exact max of the valid logits the half's intervals reach in
+// this tile (columns c0..c0+h0, still in S: P is written only once the
+// half-tile is done); O_h, when it holds this item's earlier tiles, is
+// scaled (after waiting for the previous PV) by the factor returned.
+// Returns (factor, new max); the factor is 0 when that wait expired (the
+// abort flag is then raised).
+__device__ __noinline__ float2 raise_running_max(uint32_t tS, uint32_t tO, int c0, int h0,
+                                                 int ncol_o, int c_last, float k2, float m,
+                                                 bool rescale_o, uint32_t odone, uint32_t parity,
+                                                 volatile int *abort_flag) {
+    float mx = m;
+#pragma unroll 1
+    for (int o = 0; o <= h0; o += 8) {
+        uint32_t t[8];
+        tmem_ld8(tS + c0 + o, t);
+        tmem_wait_ld8(t);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            mx = o + i <= h0 && c0 + o + i <= c_last ? fmaxf(mx, __uint_as_float(t[i]) * k2) : mx;
     }
-    float2 lsum = make_float2(0.0f, 0.0f), ls2 = make_float2(0.0f, 0.0f);
+    const float alpha = ex2_approx(m - mx);
+    if (rescale_o) {
+        if (!__all_sync(0xffffffffu, wait_c(odone, parity, abort_flag))) return make_float2(0.0f, mx);
+        tc_fence_after();
+#pragma unroll 1
+        for (int o = 0; o < ncol_o; o += 16) {
+            uint32_t t[16];
+            tmem_ld16(tO + o, t);
+            tmem_wait_ld16(t);
 #pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-        const int k = 2 * half + kk;
-        float sv[33];
+            for (int i = 0; i < 16; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+            tmem_st16(tO + o, t);
+        }
+        tmem_wait_st();
+    }
+    return make_float2(alpha, mx);
+}
+
+// One column half of one key tile for this thread's row: the weights of the
+// half's keys (columns kb..kb+h0-1, kb = h h0), held as bf16 in registers,
+// checked, then written as P_h over the half's own S columns (64 keys,
+// zero beyond the half).  Returns false if a wait expired.
+template <int D, bool SHORT, bool SYM, bool MASKED>
+__device__ __forceinline__ bool half_tile(uint32_t tS, uint32_t tO, RowState &st, int h,
+                                          int c_last, bool first, bool rescale_o, uint32_t odone,
+                                          uint32_t parity, volatile int *abort_flag) {
+    using C = TcCfg<D>;
+    constexpr int NK = C::kNK, H0 = C::kH0, NL = H0 - 48;
+    const int kb = h * H0;
+    // two chunks: 32 keys, then the remaining NB2 (24 or 32)
+    constexpr int NB2 = H0 - 32;
+    uint32_t pkA[16], pkB[NB2 / 2];
+    float2 tsum = make_float2(0.0f, 0.0f);
+    float w1 = 0.0f;
+    bool ok = true;
+    for (int attempt = 0;; ++attempt) {
+        // lg[0]: column kb-1 (0 for half 0), lg[1 + i]: column kb + i,
+        // lg[h0 + 1]: column kb + h0 (NK-1 for half 1)
+        float lg[H0 + 2];
+        uint32_t r2[16], r3[NL], r4[1];
+        {
+            uint32_t t0[1], t1[32], t2[1];
+            tmem_ld1(tS + (h ? kb - 1 : 0), t0[0]);
+            tmem_ld32(tS + kb, t1);
+            tmem_ld1(tS + kb + 32, t2[0]);
+            tmem_wait_ld_regs<1>(t0);
+            tmem_wait_ld_regs<32>(t1);
+            tmem_wait_ld_regs<1>(t2);
+            lg[0] = __uint_as_float(t0[0]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(a[kk][i]);
-        if (kk == 0)
-            sv[32] = __uint_as_float(a[1][0]);
-        else
-            sv[32] = half == 0 ? __uint_as_float(nb) : sv[31];  // column 64, or unused
-        if (k == 0 && sink == 1) sv[0] = sv[1];       // k_0 = k_1
-        if (k == 0 && sink == 2) sv[0] = st.s_sink;   // given k_0
-        float w[32], L31;
-        if (SHORT) {
-            short_chunk<MASKED>(sv, Lc, k2, nm, 32 * k, c_last, k == 0 && tile0, w);
-            L31 = sv[30];  // column 126 when k == 3
-            Lc = sv[31];   // left neighbour of the next chunk
-        } else {
-            cont_chunk<MASKED, SYM>(sv, k2, nm, 32 * k, c_last, k == 0 && tile0, Lc, L31, w);
-        }
-        if (k == 3) {
-            Lc = L31;  // carried to the next tile's first key
-            w[31] = 0.0f;
-        }
-        if (k == 0 && sink == 1) {  // v_0 = v_1: the sink's weight lands on key 1
-            w[1] += w[0];
-            w[0] = 0.0f;
-        }
-        if (k == 0 && sink == 2) {  // w_0 * v0 is added in fp32 at the end
-            st.w_sink = w[0];
-            w[0] = 0.0f;
-            st.l_run += st.w_sink;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-            pk[i >> 1] = pack_bf16x2(w[i], w[i + 1]);
-            if ((i & 2) == 0)
-                lsum = __fadd2_rn(lsum, make_float2(w[i], w[i + 1]));
+            for (int i = 0; i < 32; ++i) lg[1 + i] = __uint_as_float(t1[i]);
+            lg[33] = __uint_as_float(t2[0]);
+            // the rest of the half, read while the first chunk is computed
+            tmem_ld16(tS + kb + 32, r2);
+            if constexpr (NL == 8)
+                tmem_ld8(tS + kb + 48, r3);
             else
-                ls2 = __fadd2_rn(ls2, make_float2(w[i], w[i + 1]));
+                tmem_ld16(tS + kb + 48, r3);
+            tmem_ld1(tS + (h ? NK - 1 : H0), r4[0]);
         }
-        tmem_st16(tS + p_col(k), pk);
+        const float nm = -st.m;
+        // the share key kb receives from interval (kb-1, kb) (exact), or the
+        // u of column kb-1 (short); for half 0, column 0 is a halo: unused
+        float carry;
+        if (SHORT) {
+            carry = fmaf(lg[0], st.k2, nm);
+        } else {
+            const float u0 = fmaf(lg[0], st.k2, nm), u1 = fmaf(lg[1], st.k2, nm);
+            float R, L;
+            seg_weights(u1 - u0, ex2_approx(u0), ex2_approx(u1), R, L);
+            carry = (!MASKED || kb <= c_last) ? -L : 0.0f;
+        }
+        tsum = make_float2(0.0f, 0.0f);
+        bool bad = false;
+        auto chunk = [&](auto nck, auto edge_l, auto edge_r, int off, auto &pk) {
+            constexpr int NC = decltype(nck)::value;
+            constexpr bool EL = decltype(edge_l)::value, ER = decltype(edge_r)::value;
+            float s[NC + 1];
+#pragma unroll
+            for (int i = 0; i <= NC; ++i) s[i] = lg[1 + off + i];
+            float2 cs;
+            float w1c;
+            if (SHORT)
+                short_chunk<NC, MASKED, EL, ER>(s, st, nm, kb + off, c_last, h == 0, first && h == 0,
+                                                h == 1, carry, pk, cs, w1c);
+            else
+                cont_chunk<NC, MASKED, SYM, EL, ER>(s, st, nm, kb + off, c_last, h == 0,
+                                                   first && h == 0, h == 1, carry, pk, cs, w1c);
+            if (EL) w1 = w1c;
+            tsum = __fadd2_rn(tsum, cs);
+            bad |= !(cs.x + cs.y < kSumLimit);
+        };
+        using T_ = std::true_type;
+        using F_ = std::false_type;
+        chunk(std::integral_constant<int, 32>{}, T_{}, F_{}, 0, pkA);
+        tmem_wait_ld16(r2);
+        if constexpr (NL == 8)
+            tmem_wait_ld8(r3);
+        else
+            tmem_wait_ld16(r3);
+        tmem_wait_ld_regs<1>(r4);
+#pragma unroll
+        for (int i = 1; i < 16; ++i) lg[33 + i] = __uint_as_float(r2[i]);
+#pragma unroll
+        for (int i = 0; i < NL; ++i) lg[49 + i] = __uint_as_float(r3[i]);
+        lg[H0 + 1] = __uint_as_float(r4[0]);
+        chunk(std::integral_constant<int, NB2>{}, F_{}, T_{}, 32, pkB);
+        if (attempt > 0 || !__any_sync(0xffffffffu, bad)) break;
+        // the weights outgrew the running max: raise it, rescale O_h, redo
+        const float2 am = raise_running_max(tS, tO, kb - h, H0, C::kN, c_last, st.k2, st.m,
+                                            rescale_o, odone, parity, abort_flag);
+        if (*abort_flag) {
+            ok = false;
+            break;
+        }
+        st.l *= am.x;
+        st.w_sink *= am.x;
+        st.m = am.y;
+    }
+    if (!ok) return false;
+    if (!SYM && first && h == 0 && st.mode == CSA_K0_GIVEN) {
+        st.w_sink = w1;
+        st.l += w1;
+    }
+    // P_h: 64 keys over the half's own S columns, zero where they reach
+    // into the other half
+    const uint32_t pb = tS + C::col_p(h);
+    if constexpr (NL == 8) {
+        const uint32_t rb = pb + (h ? 4u : 0u);
+        uint32_t a8[8], a4[4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a8[i] = pkB[i];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a4[i] = pkB[8 + i];
+        tmem_st16(rb, pkA);
+        tmem_st8(rb + 16, a8);
+        tmem_st4(rb + 24, a4);
+        const uint32_t z[4] = {0u, 0u, 0u, 0u};
+        tmem_st4(pb + (h ? 0u : 28u), z);
+    } else {
+        uint32_t b16[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) b16[i] = pkB[i % (NB2 / 2)];
+        tmem_st16(pb, pkA);
+        tmem_st16(pb + 16, b16);
     }
     tmem_wait_st();
-    lsum = __fadd2_rn(lsum, ls2);
-    st.l_run += lsum.x + lsum.y;
+    st.l += tsum.x + tsum.y;
+    return true;
 }
 
 template <int D, bool SHORT, bool SYM>
@@ -445,6 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
     using C = TcCfg<D>;
     constexpr int NSK = C::kStagesK, NSV = C::kStagesV;
+    constexpr int KS = C::kKS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -454,11 +725,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #define BAR(i) (bars + 8u * (uint32_t)(i))
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+    // the item ring: query tiles taken by the producer, decoded, read by every role
+    volatile int *item_ring = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = p.T;
-    // the item ring: query tiles taken by the producer, decoded, read by every role
-    volatile int *item_ring = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 8);
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(C::kBarQ), 1);
@@ -472,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(BAR(C::kBarSFull + 0), 1);
         mbar_init(BAR(C::kBarSFull + 1), 1);
-        mbar_init(BAR(C::kBarPFull), 256);
+        for (int i = 0; i < 4; ++i) mbar_init(BAR(C::kBarPFull + i), 128);
         mbar_init(BAR(C::kBarODone), 1);
         mbar_init(BAR(C::kBarDrain), 1);
         mbar_init(BAR(C::kBarX), 256);
@@ -488,10 +759,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpProducer) {
         // The ones box of every V stage: in swizzled row r (a key of the
         // tile), logical 16-byte chunk 0 holds (1, 0, .., 0) and chunk 1
-        // zeros, so B columns d..d+15 of the PV product are (1, 0, .., 0).
+        // zeros, so B columns d..d+15 of the PV products are (1, 0, .., 0).
         for (int s = 0; s < NSV; ++s) {
-            uint8_t *ones = smem + C::kOffV + s * C::kVStageBytes + C::kTileBytes;
-            for (int r = lane; r < 128; r += 32) {
+            uint8_t *ones = smem + C::kOffV + s * C::kVBytes + C::kKBytes;
+            for (int r = lane; r < C::kNK; r += 32) {
                 *reinterpret_cast<uint4 *>(ones + r * 128 + ((0 ^ (r & 7)) << 4)) =
                     make_uint4(0x3F80u, 0u, 0u, 0u);  // bf16 1.0 in element 0
                 *reinterpret_cast<uint4 *>(ones + r * 128 + ((1 ^ (r & 7)) << 4)) =
@@ -530,11 +801,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued_q = 0, issued_k = 0, issued_v = 0;  // loads issued (K, V: tiles)
             bool ok = true;
             for (int c = 0; ok; ++c) {
-                ok = wait_c(BAR(C::kBarItemEmpty + (c & 1)), ((c >> 1) & 1) ^ 1, abort_flag);
+                ok = wait_s(BAR(C::kBarItemEmpty + (c & 1)), ((c >> 1) & 1) ^ 1, abort_flag);
                 if (!ok) break;
                 const bool last = item >= p.num_items;
                 TcItem w = {0, 0, 0};
-                if (!last) w = tc_item(item, p);
+                if (!last) w = tc_item<KS>(item, p);
                 volatile int *e = item_ring + 3 * (c & 1);
                 e[0] = w.bh;
                 e[1] = w.row0;
@@ -546,30 +817,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // it (those reads follow the Q load they wait for, so QRead
                 // cannot run a phase ahead of this wait)
                 if (c > 0) {
-                    ok = wait_c(BAR(C::kBarQEmpty), (c - 1) & 1, abort_flag) &&
-                         (p.mode != 2 || wait_c(BAR(C::kBarQRead), (c - 1) & 1, abort_flag));
+                    ok = wait_s(BAR(C::kBarQEmpty), (c - 1) & 1, abort_flag) &&
+                         (p.mode != CSA_K0_GIVEN || wait_s(BAR(C::kBarQRead), (c - 1) & 1, abort_flag));
                     if (!ok) break;
                 }
-                mbar_arrive_expect_tx(BAR(C::kBarQ), C::kTileBytes);
-                for (int cc = 0; cc < C::kChunks; ++cc)
-                    tma_load_3d(sQ + cc * kChunkBytes, &tm_q, 64 * cc, w.row0, w.bh, BAR(C::kBarQ));
+                mbar_arrive_expect_tx(BAR(C::kBarQ), C::kQBytes);
+                for (int cc = 0; cc < C::kBoxes; ++cc)
+                    tma_load_3d(sQ + cc * C::kQBox, &tm_q, 64 * cc, w.row0, w.bh, BAR(C::kBarQ));
                 issued_q = c + 1;
                 for (int j = 0; j < w.n; ++j) {
-                    const int krow = 127 * j - 1;
+                    const int krow = KS * j - 2;
                     const int g = issued_k;  // this CTA's key tile count
                     const int sk = g % NSK;
-                    if (!(ok = wait_c(BAR(C::kBarKEmpty + sk), ((g / NSK) & 1) ^ 1, abort_flag))) break;
-                    mbar_arrive_expect_tx(BAR(C::kBarKFull + sk), C::kTileBytes);
-                    for (int cc = 0; cc < C::kChunks; ++cc)
-                        tma_load_3d(sK + sk * C::kTileBytes + cc * kChunkBytes, &tm_k, 64 * cc, krow,
-                                    w.bh, BAR(C::kBarKFull + sk));
+                    if (!(ok = wait_s(BAR(C::kBarKEmpty + sk), ((g / NSK) & 1) ^ 1, abort_flag))) break;
+                    mbar_arrive_expect_tx(BAR(C::kBarKFull + sk), C::kKBytes);
+                    for (int cc = 0; cc < C::kBoxes; ++cc)
+                        tma_load_3d(sK + sk * C::kKBytes + cc * C::kKBox, &tm_k, 64 * cc, krow, w.bh,
+                                    BAR(C::kBarKFull + sk));
                     issued_k = g + 1;
                     const int sv = g % NSV;
-                    if (!(ok = wait_c(BAR(C::kBarVEmpty + sv), ((g / NSV) & 1) ^ 1, abort_flag))) break;
-                    mbar_arrive_expect_tx(BAR(C::kBarVFull + sv), C::kTileBytes);
-                    for (int cc = 0; cc < C::kChunks; ++cc)
-                        tma_load_3d(sV + sv * C::kVStageBytes + cc * kChunkBytes, &tm_v, 64 * cc,
-                                    krow, w.bh, BAR(C::kBarVFull + sv));
+                    if (!(ok = wait_s(BAR(C::kBarVEmpty + sv), ((g / NSV) & 1) ^ 1, abort_flag))) break;
+                    mbar_arrive_expect_tx(BAR(C::kBarVFull + sv), C::kKBytes);
+                    for (int cc = 0; cc < C::kBoxes; ++cc)
+                        tma_load_3d(sV + sv * C::kVBytes + cc * C::kKBox, &tm_v, 64 * cc, krow, w.bh,
+                                    BAR(C::kBarVFull + sv));
                     issued_v = g + 1;
                 }
                 // the next item, taken when this CTA is about to need it
@@ -583,29 +854,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wait_bar_drain(BAR(C::kBarVFull + j % NSV), (j / NSV) & 1, &g_tc_status);
         }
         __syncwarp();
-    } else if (warp == kWarpMma) {
+      } else {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t kIdescS = make_idesc(128, 128, false);
+            constexpr uint32_t kIdescS = make_idesc(128, C::kNK, false);
             constexpr uint32_t kIdescO = make_idesc(128, C::kN, true);
             // One stream of key tiles over this CTA's items: within an item S
             // runs two tiles ahead of PV; the next item's first S wait until
             // this item's last PV is issued, since waiting for its Q must not
             // hold that PV (and the epilogue) back.  So S and PV are always
             // in the same item.
-            int c = -1, n = 0;    // the current item and its key tiles
+            int c = -1, n = 0;     // the current item and its key tiles
             int s_j = 0, p_j = 0;  // its S and PV issued
             int gs = 0, gp = 0;    // S and PV issued over all items
             // S(gs) = Q K^T into S buffer gs % 2; K tile gs is released once done
             auto issue_s = [&]() -> bool {
-                if (!wait_c(BAR(C::kBarKFull + gs % NSK), (gs / NSK) & 1, abort_flag)) return false;
+                if (!wait_s(BAR(C::kBarKFull + gs % NSK), (gs / NSK) & 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t kb = sK + (gs % NSK) * C::kTileBytes;
+                const uint32_t kb = sK + (gs % NSK) * C::kKBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    tc_mma_ss(tmem + C::col_s(gs & 1), make_sdesc(sQ + off, 16, 1024),
-                              make_sdesc(kb + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                    const uint32_t qo = (kk >> 2) * C::kQBox + (kk & 3) * 32;
+                    const uint32_t ko = (kk >> 2) * C::kKBox + (kk & 3) * 32;
+                    tc_mma_ss(tmem + C::col_s(gs & 1), make_sdesc(sQ + qo, 16, 1024),
+                              make_sdesc(kb + ko, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(BAR(C::kBarSFull + (gs & 1)));
                 tc_commit(BAR(C::kBarKEmpty + gs % NSK));
@@ -623,22 +895,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s_j = p_j = 0;
                 n = w.n;
                 if (n == 0) return true;
-                if (!wait_c(BAR(C::kBarQ), c & 1, abort_flag)) return false;
+                if (!wait_s(BAR(C::kBarQ), c & 1, abort_flag)) return false;
                 return issue_s() && (n == 1 || issue_s());
             };
             bool ok = next_item();
             while (ok && n > 0) {
-                if (!(ok = wait_c(BAR(C::kBarPFull), gp & 1, abort_flag))) break;
+                const uint32_t vb = sV + (gp % NSV) * C::kVBytes;
+                if (!(ok = wait_s(BAR(C::kBarVFull + gp % NSV), (gp / NSV) & 1, abort_flag))) break;
                 tc_fence_after();
-                // [O | rowsum] += P(gp) [V_gp | ones], P read from the TMEM of S buffer gp % 2
-                if (!(ok = wait_c(BAR(C::kBarVFull + gp % NSV), (gp / NSV) & 1, abort_flag))) break;
-                tc_fence_after();
-                const uint32_t vb = sV + (gp % NSV) * C::kVStageBytes;
+                // [O_h | rowsum] (+)= P_h [V | ones] over the 64 keys of half h,
+                // P_h read from the TMEM of S buffer gp % 2
+                for (int h = 0; h < 2 && ok; ++h) {
+                    if (!(ok = wait_s(BAR(C::kBarPFull + 2 * h + (gp & 1)), (gp >> 1) & 1, abort_flag)))
+                        break;
+                    tc_fence_after();
+                    const uint32_t row_b = h ? (uint32_t)(C::kNK - 64) * 128u : 0u;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_ts(tmem + C::kColO, tmem + C::col_s(gp & 1) + p_col(kk >> 1) + (kk & 1) * 8,
-                              make_sdesc(vb + kk * 2048, kChunkBytes, 1024), kIdescO,
-                              (p_j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_ts(tmem + C::col_o(h), tmem + C::col_s(gp & 1) + C::col_p(h) + 8 * kk,
+                                  make_sdesc(vb + row_b + kk * 2048, C::kKBox, 1024), kIdescO,
+                                  (p_j > 0 || kk > 0) ? 1u : 0u);
+                }
+                if (!ok) break;
                 tc_commit(BAR(C::kBarODone));
                 tc_commit(BAR(C::kBarVEmpty + gp % NSV));
                 ++gp;
@@ -658,20 +936,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
         // ------------------------------------------------------ softmax
-        const int half = warp >> 2, wq = warp & 3;
+        const int h = warp >> 2, wq = warp & 3;
         const int irow = wq * 32 + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const uint32_t tO = tmem + lane_off + C::kColO;
-        float *xmax = reinterpret_cast<float *>(smem + C::kOffXMax);
-        float *xcarry = reinterpret_cast<float *>(smem + C::kOffXCarry);
+        const uint32_t tO = tmem + lane_off + C::col_o(h);
         float *xfin = reinterpret_cast<float *>(smem + C::kOffXFin);
         const uint32_t xbar = BAR(C::kBarX);
-        uint32_t xe = 0;  // exchanges completed on xbar
-        int g = 0;        // key tiles of this CTA done so far
+        int g = 0;  // key tiles of this CTA done so far
         bool ok = true;
-        while (ok) {
-            // items done so far: one exchange per key tile, one more per item
-            const int c = (int)xe - g;
+        for (int c = 0; ok; ++c) {
             TcItem w;
             ok = __all_sync(0xffffffffu, take_item(c, w));
             __syncwarp();
@@ -681,33 +954,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = row0 + irow;
             RowState st;
             st.k2 = p.k2;
-            st.m_run = -INFINITY;
-            st.l_run = st.w_sink = st.s_sink = 0.0f;
-            if (half == 0) {
-                if (p.mode == 2) {
-                    ok = __all_sync(0xffffffffu, wait_c(BAR(C::kBarQ), c & 1, abort_flag));
-                    if (!ok) break;
-                    // s_sink = q_r . k0[h], from this row of the swizzled Q tile
-                    const __nv_bfloat16 *k0h = p.k0 + (size_t)(bh % p.H) * D;
-                    float acc = 0.0f;
+            st.m = -INFINITY;
+            st.l = st.w_sink = st.s_sink = 0.0f;
+            st.mode = p.mode;
+            if (!SYM && h == 0 && p.mode == CSA_K0_GIVEN) {
+                ok = __all_sync(0xffffffffu, wait_c(BAR(C::kBarQ), c & 1, abort_flag));
+                if (!ok) break;
+                // s_sink = q_r . k0[h], from this row of the swizzled Q tile
+                const __nv_bfloat16 *k0h = p.k0 + (size_t)(bh % p.H) * D;
+                float acc = 0.0f;
 #pragma unroll
-                    for (int cc = 0; cc < C::kChunks; ++cc) {
+                for (int cc = 0; cc < C::kBoxes; ++cc) {
 #pragma unroll
-                        for (int kc = 0; kc < 8; ++kc) {
-                            const uint8_t *src = smem + C::kOffQ + cc * kChunkBytes + irow * 128 +
-                                                 ((kc ^ (irow & 7)) << 4);
-                            const uint4 qv = *reinterpret_cast<const uint4 *>(src);
-                            const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(&qv);
+                    for (int kc = 0; kc < 8; ++kc) {
+                        const uint8_t *src = smem + C::kOffQ + cc * C::kQBox + irow * 128 +
+                                             ((kc ^ (irow & 7)) << 4);
+                        const uint4 qv = *reinterpret_cast<const uint4 *>(src);
+                        const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(&qv);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                acc = fmaf(__bfloat162float(qb[e]),
-                                           __bfloat162float(k0h[cc * 64 + kc * 8 + e]), acc);
-                        }
+                        for (int e = 0; e < 8; ++e)
+                            acc = fmaf(__bfloat162float(qb[e]),
+                                       __bfloat162float(k0h[cc * 64 + kc * 8 + e]), acc);
                     }
-                    st.s_sink = acc;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(BAR(C::kBarQRead));
                 }
+                st.s_sink = acc;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(C::kBarQRead));
             }
             for (int j = 0; ok && j < n; ++j, ++g) {
                 const uint32_t tS = tmem + lane_off + C::col_s(g & 1);
@@ -716,123 +988,68 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 // last valid column of this row, and whether the tile needs masks
-                const int c_last = r + 1 - 127 * j;
-                const bool masked = 127 * j + 127 > row0 + 1;
-                const int sink = j == 0 ? p.mode : 0;
-                // this half's 64 logits and its neighbour column (64 or 63)
-                uint32_t a[2][32];
-                uint32_t nb[1] = {0u};
-                tmem_ld32(tS + 64 * half, a[0]);
-                tmem_ld32(tS + 64 * half + 32, a[1]);
-                tmem_ld1(tS + (half == 0 ? 64 : 63), nb[0]);
-                tmem_wait_ld_regs<32>(a[0]);
-                tmem_wait_ld_regs<32>(a[1]);
-                tmem_wait_ld_regs<1>(nb);
-                float s0 = __uint_as_float(a[0][0]);
-                if (half == 0 && sink == 1) s0 = __uint_as_float(a[0][1]);
-                if (half == 0 && sink == 2) s0 = st.s_sink;
-                // the symmetric interval has no sink: its logit must not raise the max
-                if (SYM && half == 0 && j == 0) s0 = -INFINITY;
-                const float mine = masked ? half_max<true>(a, half, c_last, s0)
-                                          : half_max<false>(a, half, c_last, s0);
-                // exchange the partial maxima (and the carried L share) with the other half
-                const int slot = xe & 1;
-                xmax[(slot * 2 + half) * 128 + irow] = mine;
-                mbar_arrive(xbar);
-                ok = __all_sync(0xffffffffu, wait_c(xbar, xe & 1, abort_flag));
-                ++xe;
+                const int c_last = r + 2 - KS * j;
+                const bool masked = KS * (j + 1) > row0 + 1;
+                if (j == 0) st.m = first_tile_max<SYM>(tS, st, h * (C::kH0 - 1), C::kH0, c_last);
+                const uint32_t odone = BAR(C::kBarODone), par = (g - 1) & 1;
+                ok = masked ? half_tile<D, SHORT, SYM, true>(tS, tO, st, h, c_last, j == 0, j > 0,
+                                                             odone, par, abort_flag)
+                            : half_tile<D, SHORT, SYM, false>(tS, tO, st, h, c_last, j == 0, j > 0,
+                                                              odone, par, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                const float mx = fmaxf(mine, xmax[(slot * 2 + (half ^ 1)) * 128 + irow]);
-                float Lc = 0.0f;
-                if (half == 0 && j > 0) Lc = xcarry[slot * 128 + irow];
-                const float mt = (!masked || c_last >= 0) ? mx * st.k2 : -INFINITY;
-                float alpha = 1.0f;
-                const bool grow = mt > st.m_run + 8.0f;
-                if (grow) {
-                    alpha = ex2_approx(st.m_run - mt);
-                    st.m_run = mt;
-                    st.l_run *= alpha;
-                    st.w_sink *= alpha;
-                    if (!SHORT) Lc *= alpha;  // SHORT carries a raw logit
-                }
-                const float nm = -st.m_run;
-                if (masked)
-                    half_weights<true, SHORT, SYM>(tS, a, nb[0], st, half, c_last, sink, j == 0, nm, Lc);
-                else
-                    half_weights<false, SHORT, SYM>(tS, a, nb[0], st, half, c_last, sink, j == 0, nm, Lc);
-                if (half == 1) xcarry[(xe & 1) * 128 + irow] = Lc;
-                // Rescale O (this half's value columns; half 1 also the row-sum
-                // column) when the max moved, after PV of the previous tile finished.
-                const bool need_o = grow && j > 0;
-                if (__any_sync(0xffffffffu, need_o)) {
-                    ok = __all_sync(0xffffffffu, wait_c(BAR(C::kBarODone), (g - 1) & 1, abort_flag));
-                    if (!ok) break;
-                    tc_fence_after();
-                    const float s = need_o ? alpha : 1.0f;
-#pragma unroll
-                    for (int cc = 0; cc < D / 64; ++cc) {
-                        uint32_t o[32];
-                        const uint32_t ta = tO + half * (D / 2) + 32 * cc;
-                        tmem_ld32(ta, o);
-                        tmem_wait_ld_regs<32>(o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * s);
-                        tmem_st32(ta, o);
-                    }
-                    if (half == 1) {
-                        uint32_t o[1];
-                        tmem_ld1(tO + D, o[0]);
-                        tmem_wait_ld_regs<1>(o);
-                        o[0] = __float_as_uint(__uint_as_float(o[0]) * s);
-                        tmem_st1(tO + D, o[0]);
-                    }
-                    tmem_wait_st();
-                }
                 tc_fence_before();
-                mbar_arrive(BAR(C::kBarPFull));
+                mbar_arrive(BAR(C::kBarPFull + 2 * h + (g & 1)));
             }
             if (!ok) break;
-            // combine the two halves' fp32 sums; the given sink's weight lives in half 0
-            float *mine = xfin + (half * 128 + irow) * 2;
-            mine[0] = st.l_run;
-            mine[1] = st.w_sink;
+            // the two halves meet: their maxima, sums and the given sink's weight
+            float *mine = xfin + (h * 128 + irow) * 4;
+            mine[0] = st.m;
+            mine[1] = st.l;
+            mine[2] = st.w_sink;
             mbar_arrive(xbar);
             // sleeping: the MMA thread is issuing this item's last PV meanwhile
-            ok = __all_sync(0xffffffffu, wait_s(xbar, xe & 1, abort_flag));
-            ++xe;
+            ok = __all_sync(0xffffffffu, wait_s(xbar, c & 1, abort_flag));
             if (!ok) break;
-            const float *oth = xfin + ((half ^ 1) * 128 + irow) * 2;
-            const float l_run = st.l_run + oth[0];
-            const float w_sink = half == 0 ? st.w_sink : oth[1];
+            const float *oth = xfin + ((h ^ 1) * 128 + irow) * 4;
+            const float m0 = h ? oth[0] : st.m, m1 = h ? st.m : oth[0];
+            const float l0 = h ? oth[1] : st.l, l1 = h ? st.l : oth[1];
+            const float w_sink = h ? oth[2] : st.w_sink;  // in half 0's scale
+            const float mx = fmaxf(m0, m1);
+            const float a0 = ex2_approx(m0 - mx), a1 = ex2_approx(m1 - mx);
             // O holds this item's last PV once it is done; the next item's
             // first PV waits for this thread's PFull arrival, after the reads
             ok = __all_sync(0xffffffffu, wait_s(BAR(C::kBarODone), (g - 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
+            const uint32_t tO0 = tmem + lane_off + C::col_o(0), tO1 = tmem + lane_off + C::col_o(1);
             // o is divided by the sum of exactly the bf16 weights that fed the
-            // PV product (O column d) plus the given sink's fp32 weight
-            uint32_t lb[1];
-            tmem_ld1(tO + D, lb[0]);
-            tmem_wait_ld_regs<1>(lb);
-            const float inv_l = 1.0f / (__uint_as_float(lb[0]) + w_sink);
+            // PV products (column d of each O_h) plus the given sink's fp32 weight
+            uint32_t rs[2][1];
+            tmem_ld1(tO0 + D, rs[0][0]);
+            tmem_ld1(tO1 + D, rs[1][0]);
+            tmem_wait_ld_regs<1>(rs[0]);
+            tmem_wait_ld_regs<1>(rs[1]);
+            const float den = fmaf(a0, __uint_as_float(rs[0][0]) + w_sink, a1 * __uint_as_float(rs[1][0]));
+            const float inv_l = 1.0f / den;
             const bool store = r < T;
             __nv_bfloat16 *orow =
-                p.out + ((size_t)bh * T + (size_t)(store ? r : 0)) * D + half * (D / 2);
-            const __nv_bfloat16 *v0h = p.v0 + (size_t)(bh % p.H) * D + half * (D / 2);
-            uint32_t oc[D / 64][32];
-#pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc) tmem_ld32(tO + half * (D / 2) + 32 * cc, oc[cc]);
-#pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc) tmem_wait_ld_regs<32>(oc[cc]);
+                p.out + ((size_t)bh * T + (size_t)(store ? r : 0)) * D + h * (D / 2);
+            const __nv_bfloat16 *v0h = p.v0 + (size_t)(bh % p.H) * D + h * (D / 2);
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
-                const uint32_t *o = oc[cc];
+                uint32_t o0[32], o1[32];
+                tmem_ld32(tO0 + h * (D / 2) + 32 * cc, o0);
+                tmem_ld32(tO1 + h * (D / 2) + 32 * cc, o1);
+                tmem_wait_ld_regs<32>(o0);
+                tmem_wait_ld_regs<32>(o1);
                 float val[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    float x = __uint_as_float(o[e]);
-                    if (p.mode == 2) x = fmaf(w_sink, __bfloat162float(v0h[32 * cc + e]), x);
-                    val[e] = x * inv_l;
+                    float xo = __uint_as_float(o0[e]);
+                    if (!SYM && p.mode == CSA_K0_GIVEN)
+                        xo = fmaf(w_sink, __bfloat162float(v0h[32 * cc + e]), xo);
+                    val[e] = fmaf(a0, xo, a1 * __uint_as_float(o1[e])) * inv_l;
                 }
                 uint32_t pk[16];
 #pragma unroll
@@ -844,9 +1061,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                 }
             }
-            if (store && half == 0 && p.lse)
+            if (store && h == 0 && p.lse)
                 p.lse[(size_t)bh * T + r] =
-                    (st.m_run + log2f(l_run)) * kLn2 + (SHORT ? 0.0f : kLseShift);
+                    (mx + log2f(fmaf(a0, l0, a1 * l1))) * kLn2 + (SHORT ? 0.0f : kLseShift);
             tc_fence_before();
         }
     }
@@ -941,8 +1158,8 @@ int launch_tc(const void *q, const void *k, const void *v, const void *k0, const
     using C = TcCfg<D>;
     const int BH = B * H;
     CUtensorMap mq, mk, mv;
-    if (!encode_qkv_map(&mq, q, BH, T, D) || !encode_qkv_map(&mk, k, BH, T, D) ||
-        !encode_qkv_map(&mv, v, BH, T, D))
+    if (!encode_qkv_map(&mq, q, BH, T, D) || !encode_rows_map(&mk, k, BH, T, D, C::kNK) ||
+        !encode_rows_map(&mv, v, BH, T, D, C::kNK))
         return CSA_ERR_CUDA;
     TcParams prm;
     prm.B = B;

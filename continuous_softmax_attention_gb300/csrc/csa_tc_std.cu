@@ -77,9 +77,16 @@ __device__ __forceinline__ bool wait_s(uint32_t bar, uint32_t parity, volatile i
     return wait_bar(bar, parity, abort_flag, &g_std_status);
 }
 
+__device__ __forceinline__ float fmin3f(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Softmax of one S tile at tS for this thread's row.  Returns whether the
-// running max moved (alpha is then the factor O must be scaled by).
-template <bool MASKED>
+// running max moved (alpha is then the factor O must be scaled by).  NEG:
+// the scale is negative, so the largest scaled logit is the smallest q.k.
+template <bool MASKED, bool NEG>
 __device__ __forceinline__ bool std_tile(uint32_t tS, float k2, int c_last, float &m_run,
                                          float &l_run, float &alpha) {
     float mx;
@@ -89,20 +96,24 @@ __device__ __forceinline__ bool std_tile(uint32_t tS, float k2, int c_last, floa
         for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + 32 * cc, sr[cc]);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) tmem_wait_ld_regs<32>(sr[cc]);
+        constexpr float kNone = NEG ? INFINITY : -INFINITY;
         float a[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = -INFINITY;
+        for (int i = 0; i < 8; ++i) a[i] = kNone;
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
             float v0 = __uint_as_float(sr[c >> 5][c & 31]);
             float v1 = __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]);
             if (MASKED) {
-                v0 = c <= c_last ? v0 : -INFINITY;
-                v1 = c + 1 <= c_last ? v1 : -INFINITY;
+                v0 = c <= c_last ? v0 : kNone;
+                v1 = c + 1 <= c_last ? v1 : kNone;
             }
-            a[(c >> 1) & 7] = fmax3f(a[(c >> 1) & 7], v0, v1);
+            a[(c >> 1) & 7] = NEG ? fmin3f(a[(c >> 1) & 7], v0, v1) : fmax3f(a[(c >> 1) & 7], v0, v1);
         }
-        mx = fmax3f(fmax3f(a[0], a[1], a[2]), fmax3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+        if (NEG)
+            mx = fmin3f(fmin3f(a[0], a[1], a[2]), fmin3f(a[3], a[4], a[5]), fminf(a[6], a[7]));
+        else
+            mx = fmax3f(fmax3f(a[0], a[1], a[2]), fmax3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
     }
     const float mt = (!MASKED || c_last >= 0) ? mx * k2 : -INFINITY;
     alpha = 1.0f;
@@ -328,9 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int c_last = r - 128 * j;
             float alpha;
-            const bool grow = (128 * j + 127 > row0[qt])
-                                  ? std_tile<true>(tS, p.k2, c_last, m_run, l_run, alpha)
-                                  : std_tile<false>(tS, p.k2, c_last, m_run, l_run, alpha);
+            const bool masked = 128 * j + 127 > row0[qt];
+            const bool grow =
+                p.k2 < 0.0f
+                    ? (masked ? std_tile<true, true>(tS, p.k2, c_last, m_run, l_run, alpha)
+                              : std_tile<false, true>(tS, p.k2, c_last, m_run, l_run, alpha))
+                    : (masked ? std_tile<true, false>(tS, p.k2, c_last, m_run, l_run, alpha)
+                              : std_tile<false, false>(tS, p.k2, c_last, m_run, l_run, alpha));
             const bool need_o = grow && j > 0;
             if (__any_sync(0xffffffffu, need_o)) {
                 ok = __all_sync(0xffffffffu, wait_s(BAR(C::kBarODone + qt), (j - 1) & 1, abort_flag));

@@ -94,8 +94,8 @@ enum {
  *   q, k, v, k0, v0: bf16 (__nv_bfloat16); out: bf16; lse: float.
  *   Accumulation and the correction b are computed in fp32.
  *   d = 64 or 128 runs the tcgen05/TMA kernel; any other 1 <= d <= 256 runs
- *   the CUDA-core kernel.  d > 256: CSA_ERR_UNSUPPORTED.  scale < 0 on the
- *   tensor-core kernel: CSA_ERR_UNSUPPORTED.
+ *   the CUDA-core kernel.  d > 256: CSA_ERR_UNSUPPORTED.  Any finite scale,
+ *   of either sign, on both kernels.
  *   q, k, v, out must be 16-byte aligned (CSA_ERR_ALIGNMENT otherwise).
  *   k0, v0 are read only in CSA_K0_GIVEN mode and may be NULL otherwise.
  */

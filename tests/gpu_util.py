@@ -38,9 +38,11 @@ def assert_close(o, lse, ro, rl, dtype, what=""):
 
 
 def boundary_rows(T, extra=()):
-    """Rows around every tile edge of both kernels (stride 127 and 128)."""
+    """Rows around every tile edge of the kernels: query tiles of 128 rows
+    (pairs of 256), key tiles every 110 (d = 128) or 126 (d = 64) keys, and
+    the 128-key tiles of the standard kernel."""
     rows = set(extra)
-    for base in (127, 128, 256):
+    for base in (110, 126, 128, 256):
         n = 1
         while base * n - 2 < T:
             for dlt in (-2, -1, 0, 1):

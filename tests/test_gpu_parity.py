@@ -66,9 +66,13 @@ def test_std_f32_kernel(T, d):
 
 
 # ------------------------------------------------------------------ bf16 tensor cores
-TC_SHAPES = [(128, 1), (128, 2), (128, 3), (128, 126), (128, 127), (128, 128), (128, 129),
+# Lengths around every tile edge of the tensor-core kernels: 128-row query
+# tiles in 256-row pairs, key tiles every 110 keys (d = 128) or 126 (d = 64).
+TC_SHAPES = [(128, 1), (128, 2), (128, 3), (128, 108), (128, 109), (128, 110), (128, 111),
+             (128, 126), (128, 127), (128, 128), (128, 129), (128, 219), (128, 220), (128, 221),
              (128, 254), (128, 255), (128, 256), (128, 257), (128, 383), (128, 385), (128, 700),
-             (64, 1), (64, 5), (64, 127), (64, 255), (64, 258), (64, 513)]
+             (64, 1), (64, 5), (64, 124), (64, 125), (64, 126), (64, 127), (64, 128), (64, 251),
+             (64, 252), (64, 255), (64, 258), (64, 513)]
 
 
 @pytest.mark.parametrize("d,T", TC_SHAPES)
@@ -159,7 +163,8 @@ def test_determinism():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-@pytest.mark.parametrize("cut", [0, 125, 126, 127, 128, 253, 254, 255, 300])
+@pytest.mark.parametrize("cut", [0, 107, 108, 109, 110, 125, 126, 127, 128, 217, 218, 219, 253, 254,
+                                 255, 300])
 def test_causality_no_halo_leak(cut):
     """Changing keys/values after position `cut` leaves rows <= cut bit-identical
     (the halo column must not see past the diagonal)."""
@@ -207,8 +212,42 @@ def test_no_lse_requested():
     assert np.abs(np64(o) - ro).max() < 2e-2
 
 
-def test_scale_negative_rejected_on_tensor_cores():
-    x = make_inputs(1, 1, 16, 64, "bf16", seed=10)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("scale", [-0.1, -1.0])
+@pytest.mark.parametrize("mode", MODES)
+def test_negative_scale(d, scale, mode):
+    """The pages put no sign on the logits (eq. (2)): a negative scale runs on
+    the tensor cores like any other."""
+    x = make_inputs(1, 3, 300, d, "bf16", seed=10 + d)
+    o, lse = run_csa(x, mode, scale)
+    ro, rl = oracle_csa(x, mode, scale)
+    assert_close(o, lse, ro, rl, "bf16", f"scale={scale} mode={mode} d={d}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_std_negative_scale(d):
+    x = make_inputs(1, 2, 300, d, "bf16", seed=20 + d)
     g = to_dev(x)
-    with pytest.raises(csa.CsaError):
-        csa.forward(g["q"], g["k"], g["v"], scale=-0.1)
+    o, lse = csa.std_forward(g["q"], g["k"], g["v"], scale=-0.3)
+    torch.cuda.synchronize()
+    ro, rl = oracle.std_forward(x["q"], x["k"], x["v"], scale=-0.3)
+    assert_close(o, lse, ro, rl, "bf16", f"std scale<0 d={d}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mode", MODES)
+def test_running_max_raised(d, mode):
+    """Keys far into the sequence whose logits exceed every earlier one by
+    hundreds (log2 units): the kernel holds the first key tile's max until a
+    16-key chunk's weights would pass 2^64, then raises it and rescales what
+    it has written.  The oracle is exact for any logits."""
+    T = 700
+    x = make_inputs(1, 2, T, d, "bf16", seed=30 + d)
+    k = x["k"].float()
+    for pos, f in ((300, 25.0), (301, 25.0), (450, 60.0), (640, 90.0)):
+        k[:, :, pos] = k[:, :, pos] * f
+    x["k"] = k.to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_csa(x, mode, scale)
+    ro, rl = oracle_csa(x, mode, scale)
+    assert_close(o, lse, ro, rl, "bf16", f"max raised d={d} mode={mode}")

@@ -30,7 +30,7 @@ def test_short_conv_f32(mode):
 
 @pytest.mark.parametrize("d", [64, 128, 96])
 @pytest.mark.parametrize("mode", [0, 1, 2])
-@pytest.mark.parametrize("T", [1, 2, 127, 128, 300, 700])
+@pytest.mark.parametrize("T", [1, 2, 109, 110, 111, 127, 128, 221, 300, 700])
 def test_short_conv_bf16(d, mode, T):
     x = make_inputs(1, 2, T, d, "bf16", seed=210 + T + d + mode)
     scale = 1.0 / d ** 0.5

@@ -26,7 +26,7 @@ def test_symmetric_f32():
 
 
 @pytest.mark.parametrize("d", [64, 128, 96])
-@pytest.mark.parametrize("T", [1, 2, 3, 126, 127, 128, 129, 254, 255, 300, 700])
+@pytest.mark.parametrize("T", [1, 2, 3, 109, 110, 111, 126, 127, 128, 129, 220, 254, 255, 300, 700])
 def test_symmetric_bf16(d, T):
     x = make_inputs(1, 2, T, d, "bf16", seed=310 + T + d)
     scale = 1.0 / d ** 0.5
