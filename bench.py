@@ -28,14 +28,27 @@ Also reported on the same JSON line:
                queries from pinned host memory, outputs back to the host;
                the cache stays resident as it would while serving)
   backward     the backward pass (csa_backward) at the same shape
-  workloads    the continuous and standard kernels at the mid (4 x 16 x
-               2048 x 128, RoPE) and long (1 x 8 x 32768 x 64, per-head
-               sink) workloads
+  workloads    every other workload of the evaluation plan: the continuous
+               and standard kernels at the mid (4 x 16 x 2048 x 128, RoPE)
+               and long (1 x 8 x 32768 x 64, per-head sink) workloads, with
+               tokens/s and an oracle baseline on sampled rows; the tiny
+               (fp32, 1 x 1 x 64 x 16) and stress (2 x 4 x 512 x 64, scale
+               x sink-mode sweep) workloads with the oracle's full run timed
+               beside them
 
 `--impl reference` times the CPU oracle alone (the reference arm).
-Multi-GPU (torchrun): every rank runs its own copy of the workload (the
-(b, h) problems are independent; no collective on the data path), the time
-is the max over ranks, and value = all ranks' flops / that time.
+Multi-GPU (torchrun), two modes:
+  default      weak scaling of replicas: every rank runs its own copy of the
+               workload (the (b, h) problems are independent; no collective
+               on the data path), the time is the max over ranks, and value
+               = all ranks' flops / that time
+  --shard      strong scaling: the headline's B*H problems are split into N
+               contiguous shards (continuous_softmax_attention_gb300.dist:
+               the partition forward_sharded uses, no gather in the timed
+               region), each rank times the forward and standard kernels on
+               its shard, and value = the whole workload's flops / the max
+               over ranks; the decode, backward and other-workload legs are
+               left out
 """
 from __future__ import annotations
 
@@ -179,6 +192,32 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def run_shard_plan(args, ws, rank):
+    """Without a GPU (gloo): the partition --shard times, every rank's
+    [start, stop) of the headline's flattened (b, h) problems gathered to
+    rank 0.  Checks the argument handling and the partition; nothing is
+    timed and nothing is computed."""
+    import torch.distributed as dist
+
+    from continuous_softmax_attention_gb300.dist import head_shard
+    from continuous_softmax_attention_gb300.inputs import WORKLOADS
+
+    w = WORKLOADS[WORKLOAD]
+    n = w.B * w.H
+    mine = head_shard(n, ws, rank) if args.shard else (0, n)
+    ranges = [mine]
+    if ws > 1:
+        ranges = [None] * ws
+        dist.all_gather_object(ranges, mine)
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+    return {"plan": "shard" if args.shard else "replicas", "n_gpus": ws,
+            "scaling": "strong" if args.shard else "weak",
+            "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "T": w.T, "d": w.d},
+            "ranges": [list(r) for r in ranges], "timed": False}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -189,20 +228,35 @@ def run_gpu(args):
 
     ws, rank, local = _dist_env()
     if ws > 1:
-        dist.init_process_group("nccl")
+        dist.init_process_group(args.backend)
+    if args.backend == "gloo" and not torch.cuda.is_available():  # argument handling only
+        return run_shard_plan(args, ws, rank)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = WORKLOADS[WORKLOAD]
     B, H, T, d = w.B, w.H, w.T, w.d
     scale = 1.0 / math.sqrt(d)
     x = workload_inputs(WORKLOAD)
+    flops = algorithmic_flops(B, H, T, d, continuous=True)
+    flops_std = algorithmic_flops(B, H, T, d, continuous=False)
+    # per-rank work: the whole workload (replicas), or this rank's shard
+    rep_world = ws
+    if args.shard:
+        from continuous_softmax_attention_gb300.dist import shard_inputs
+
+        qs, ks, vs, k0s, v0s, (start, stop) = shard_inputs(x["q"], x["k"], x["v"], x["k0"],
+                                                           x["v0"], ws, rank)
+        x = {"q": qs.contiguous(), "k": ks.contiguous(), "v": vs.contiguous(),
+             "k0": k0s.contiguous(), "v0": v0s.contiguous()}
+        B, H = 1, stop - start
+        rep_world = 1  # every rank's flops are a share of the one workload
+        args.no_decode = args.no_backward = args.no_workloads = True
     g = {k: v.to(dev) for k, v in x.items()}
     out = torch.empty_like(g["q"])
     lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    flops = algorithmic_flops(B, H, T, d, continuous=True)
-    flops_std = algorithmic_flops(B, H, T, d, continuous=False)
+    e2e_hpc = max(c for c in range(1, min(E2E_HEADS_PER_CHUNK, H) + 1) if H % c == 0)
 
     def barrier():
         if ws > 1:
@@ -238,8 +292,7 @@ def run_gpu(args):
     pin = {k: x[k].pin_memory() for k in ("q", "k", "v")}
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    pipe = csa.HostForwardPipeline(B, H, T, d, dev, heads_per_chunk=E2E_HEADS_PER_CHUNK,
-                                   stream=stream)
+    pipe = csa.HostForwardPipeline(B, H, T, d, dev, heads_per_chunk=e2e_hpc, stream=stream)
 
     def e2e_call():
         pipe(pin["q"], pin["k"], pin["v"], host_out, host_lse, mode=w.modes[0], scale=scale)
@@ -317,12 +370,15 @@ def run_gpu(args):
         return None
     K = args.steps
     ms_step = tot_csa / K
-    value = ws * flops * K / (tot_csa * 1e-3) / 1e12
-    std_value = ws * flops_std * K / (tot_std * 1e-3) / 1e12
-    e2e_value = ws * flops * K / (tot_e2e * 1e-3) / 1e12
+    value = rep_world * flops * K / (tot_csa * 1e-3) / 1e12
+    std_value = rep_world * flops_std * K / (tot_std * 1e-3) / 1e12
+    e2e_value = rep_world * flops * K / (tot_e2e * 1e-3) / 1e12
     burst, sustained, src = _peaks()
     clocks = clk.summary()
-    achieved = flops / (ms_step * 1e-3) / 1e12
+    # the kernel's own rate: this rank's flops per launch over its time
+    rank_flops = algorithmic_flops(B, H, T, d, continuous=True)
+    rank_flops_std = algorithmic_flops(B, H, T, d, continuous=False)
+    achieved = rank_flops / (ms_step * 1e-3) / 1e12
     line = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -332,14 +388,17 @@ def run_gpu(args):
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5),
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong" if args.shard else "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "H": H, "T": T, "d": d, "scale": scale,
-                   "k0_mode": "zero", "causal": True, "per_gpu": "full workload per rank",
+        "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "T": T, "d": d, "scale": scale,
+                   "k0_mode": "zero", "causal": True,
+                   "per_gpu": (f"shard of the B*H problems ({H} of {w.B * w.H} on rank 0), "
+                               "no gather in the timed region" if args.shard else
+                               "full workload per rank (replicas)"),
                    "l2": "flushed (512 MiB write) before every timed step; inputs 192 MiB > L2"},
-        "tokens_per_s": round(ws * B * T * K / (tot_csa * 1e-3), 1),
+        "tokens_per_s": round((w.B * T if args.shard else ws * B * T) * K / (tot_csa * 1e-3), 1),
         "pct_bf16_peak": round(100.0 * achieved / burst, 2),
         "std": {"value": round(std_value, 3), "unit": UNIT, "ms_per_step": round(tot_std / K, 5),
                 "ratio_continuous_over_std": round(value / std_value, 4)},
@@ -349,21 +408,22 @@ def run_gpu(args):
                         "per pipeline chunk, two workspaces alternating: each step's copies in "
                         "overlap the previous step's kernels and copies out"),
                 "timed": "the K steps back to back as one CUDA-event region"},
-        "short_conv": {"value": round(ws * flops * K / (tot_sc * 1e-3) / 1e12, 3), "unit": UNIT,
+        "short_conv": {"value": round(rep_world * flops * K / (tot_sc * 1e-3) / 1e12, 3), "unit": UNIT,
                        "ms_per_step": round(tot_sc / K, 5),
                        "ratio_over_std": round((flops / tot_sc) / (flops_std / tot_std), 4),
                        "note": "first-order (eq. (13)) reading of the same step, csa_forward_short_conv"},
-        "symmetric": {"value": round(ws * flops_std * K / (tot_sym * 1e-3) / 1e12, 3),
+        "symmetric": {"value": round(rep_world * flops_std * K / (tot_sym * 1e-3) / 1e12, 3),
                       "unit": UNIT, "ms_per_step": round(tot_sym / K, 5),
                       "note": "eq. (2) over [1/2, t+1/2] (csa_forward_symmetric); flops over its "
                               "B*H*T(T+1)/2 pairs (no sink)"},
-        "gpu_launches": 4 * K + K * (B * H // E2E_HEADS_PER_CHUNK) +
+        "gpu_launches": 4 * K + K * (B * H // e2e_hpc) +
                         (0 if dec is None else 2 * 2 * args.decode_steps) +
                         (0 if bwd is None else bwd.launches * args.backward_steps) +
                         (0 if more is None else more.launches * args.workload_steps),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": burst,
                      "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
-                     "peak_source": f"{src} bf16 dense (burst)", "traffic": recorded_traffic(),
+                     "peak_source": f"{src} bf16 dense (burst)",
+                     "traffic": recorded_traffic() if (B, H) == (w.B, w.H) else None,
                      "traffic_unit": "bytes per launch (ncu dram read+write)",
                      "algorithmic_bytes": 2 * 4 * B * H * T * d + 4 * B * H * T},
         "clocks": clocks,
@@ -378,6 +438,8 @@ def run_gpu(args):
         line["workloads"] = more.summary(ws, args.workload_steps, burst, src)
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = cpu_baseline(x, scale, budget_s=args.cpu_seconds)
+        if more is not None:
+            more.cpu_baselines(line["workloads"])
         line["short_conv"]["cpu_baseline"] = cpu_baseline_form(x, scale, "short_conv")
         line["symmetric"]["cpu_baseline"] = cpu_baseline_form(x, scale, "symmetric")
         if bwd is not None:
@@ -388,10 +450,17 @@ def run_gpu(args):
 
 
 class WorkloadBench:
-    """The forward pass and the standard kernel at the two other timed shapes
-    of the evaluation plan: mid (B=4, H=16, T=2048, d=128, RoPE, zero sink)
-    and long (B=1, H=8, T=32768, d=64, per-head sink).  Their parity tests
-    run the same launches; this puts their throughput on the same line."""
+    """Every other workload of the evaluation plan on the same line:
+      mid    B=4, H=16, T=2048, d=128, RoPE, zero sink
+      long   B=1, H=8, T=32768, d=64, per-head sink
+    the continuous and standard kernels (the launches their parity tests
+    run), with tokens/s and, at N = 1, the oracle on rows sampled from the
+    workload; and
+      tiny   B=1, H=1, T=64, d=16, fp32 (CUDA-core kernels), scale 1/4
+      stress B=2, H=4, T=512, d=64, bf16, scale {1/8, 1, 4} x sink {zero,
+             copy-first}
+    each run timed on the GPU beside the oracle's full run of the same
+    workload (these finish in well under a second on the host)."""
 
     NAMES = ("mid", "long")
 
@@ -403,7 +472,8 @@ class WorkloadBench:
         self.legs = []
         for name in self.NAMES:
             w = WORKLOADS[name]
-            g = {k: t.to(dev) for k, t in workload_inputs(name).items()}
+            x = workload_inputs(name)
+            g = {k: t.to(dev) for k, t in x.items()}
             scale = 1.0 / math.sqrt(w.d)
             out = torch.empty_like(g["q"])
             lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
@@ -413,24 +483,61 @@ class WorkloadBench:
                                 out=out, lse=lse))
             std = (lambda g=g, scale=scale, out=out, lse=lse:
                    csa.std_forward(g["q"], g["k"], g["v"], scale=scale, out=out, lse=lse))
-            self.legs.append({"name": name, "w": w, "mode": mode, "calls": (cont, std),
+            self.legs.append({"name": name, "w": w, "mode": mode, "calls": (cont, std), "x": x,
+                              "scale": scale,
                               "flops": (algorithmic_flops(w.B, w.H, w.T, w.d, continuous=True),
                                         algorithmic_flops(w.B, w.H, w.T, w.d, continuous=False)),
                               "bytes": 3 * g["q"].numel() * 2})
-        self.launches = 2 * len(self.legs)
+        # the small workloads: one run per (scale, mode)
+        self.small = []
+        for name in ("tiny", "stress"):
+            w = WORKLOADS[name]
+            x = workload_inputs(name)
+            g = {k: t.to(dev) for k, t in x.items()}
+            scales = w.scales or (1.0 / math.sqrt(w.d),)
+            runs = []
+            for sc in scales:
+                for mode in w.modes:
+                    runs.append({"scale": sc, "mode": mode,
+                                 "call": (lambda g=g, sc=sc, mode=mode:
+                                          csa.forward(g["q"], g["k"], g["v"], g["k0"], g["v0"],
+                                                      mode=mode, scale=sc))})
+                runs[-1]["std"] = (lambda g=g, sc=sc: csa.std_forward(g["q"], g["k"], g["v"],
+                                                                      scale=sc))
+            self.small.append({"name": name, "w": w, "x": x, "runs": runs,
+                               "flops": (algorithmic_flops(w.B, w.H, w.T, w.d, continuous=True),
+                                         algorithmic_flops(w.B, w.H, w.T, w.d, continuous=False))})
+        n_small = sum(len(sm["runs"]) + sum(1 for r in sm["runs"] if "std" in r)
+                      for sm in self.small)
+        self.launches = 2 * len(self.legs) + n_small
 
     def warm(self):
         for leg in self.legs:
             for c in leg["calls"]:
                 c()
+        for sm in self.small:
+            for r in sm["runs"]:
+                r["call"]()
+                if "std" in r:
+                    r["std"]()
 
     def time(self, timed, steps):
         for leg in self.legs:
             leg["ms"] = [timed(c, steps) for c in leg["calls"]]
+        for sm in self.small:
+            for r in sm["runs"]:
+                r["ms"] = timed(r["call"], steps)
+                if "std" in r:
+                    r["ms_std"] = timed(r["std"], steps)
 
     def reduce(self, total):
         for leg in self.legs:
             leg["tot"] = [total(ms) for ms in leg["ms"]]
+        for sm in self.small:
+            for r in sm["runs"]:
+                r["tot"] = total(r["ms"])
+                if "std" in r:
+                    r["tot_std"] = total(r["ms_std"])
 
     def summary(self, world, steps, peak, src):
         out = {}
@@ -444,6 +551,7 @@ class WorkloadBench:
                            "k0_mode": ("zero", "copy_first", "given")[leg["mode"]],
                            "rope": bool(w.rope)},
                 "value": round(vc, 3), "unit": UNIT, "ms_per_step": round(tc / steps, 5),
+                "tokens_per_s": round(world * w.B * w.T * steps / (tc * 1e-3), 1),
                 "pct_bf16_peak": round(100.0 * (fc / (tc / steps * 1e-3) / 1e12) / peak, 2),
                 "peak_source": f"{src} bf16 dense (burst)",
                 "std": {"value": round(vs, 3), "ms_per_step": round(ts / steps, 5)},
@@ -451,7 +559,55 @@ class WorkloadBench:
                 "l2": (f"flushed (512 MiB write) before every timed step; q, k, v "
                        f"{leg['bytes'] / 2**20:.0f} MiB"),
             }
+        for sm in self.small:
+            w = sm["w"]
+            fc, fs = sm["flops"]
+            runs = []
+            std_of = {r["scale"]: r["tot_std"] for r in sm["runs"] if "std" in r}
+            for r in sm["runs"]:
+                ms = r["tot"] / steps
+                entry = {"scale": r["scale"], "k0_mode": ("zero", "copy_first", "given")[r["mode"]],
+                         "value": round(world * fc / (ms * 1e-3) / 1e12, 4), "ms_per_step": round(ms, 5),
+                         "tokens_per_s": round(world * w.B * w.T / (ms * 1e-3), 1),
+                         "pct_bf16_peak": round(100.0 * (fc / (ms * 1e-3) / 1e12) / peak, 4)}
+                if r["scale"] in std_of:  # the standard kernel at this scale (no sink)
+                    ms_s = std_of[r["scale"]] / steps
+                    entry["std"] = {"value": round(world * fs / (ms_s * 1e-3) / 1e12, 4),
+                                    "ms_per_step": round(ms_s, 5)}
+                    entry["ratio_continuous_over_std"] = round((fc / ms) / (fs / ms_s), 4)
+                runs.append(entry)
+            out[sm["name"]] = {
+                "config": {"B": w.B, "H": w.H, "T": w.T, "d": w.d, "dtype": w.dtype},
+                "unit": UNIT, "runs": runs,
+                "note": ("fp32 CUDA-core kernels" if w.dtype == "f32" else
+                         "bf16 tensor-core kernels") + "; small enough that launch latency "
+                        "dominates the GPU time",
+                "l2": "flushed (512 MiB write) before every timed step",
+            }
         return out
+
+    def cpu_baselines(self, line):
+        """The oracle beside each workload: sampled rows for mid and long (as
+        the headline's cpu_baseline), the full run of every tiny and stress
+        case."""
+        import oracle
+
+        cores = oracle.default_threads()
+        for leg in self.legs:
+            cb = cpu_baseline(leg["x"], leg["scale"], budget_s=4.0, mode=leg["mode"])
+            line[leg["name"]]["cpu_baseline"] = cb
+        for sm, (name, runs) in zip(self.small, ((s["name"], line[s["name"]]["runs"])
+                                                  for s in self.small)):
+            x, w = sm["x"], sm["w"]
+            fc = sm["flops"][0]
+            for r, entry in zip(sm["runs"], runs):
+                t0 = time.perf_counter()
+                oracle.forward(x["q"], x["k"], x["v"], x["k0"], x["v0"], scale=r["scale"],
+                               mode=r["mode"])
+                dt = time.perf_counter() - t0
+                entry["cpu_baseline"] = {"value": fc / dt / 1e12, "unit": UNIT, "cores": cores,
+                                         "kind": "oracle", "seconds": round(dt, 4),
+                                         "sample": "the whole workload (eq. (8) in double)"}
 
 
 class BackwardBench:
@@ -593,7 +749,7 @@ def _sample_rows(T, H, nrows, seed=0):
     return picks
 
 
-def cpu_baseline(x, scale, budget_s=15.0, seed=0):
+def cpu_baseline(x, scale, budget_s=15.0, seed=0, mode=0):
     """The oracle (eq. (8), double, all host cores) on rows sampled uniformly
     from the workload; rate = algorithmic flops of those rows / wall time."""
     import numpy as np
@@ -604,6 +760,8 @@ def cpu_baseline(x, scale, budget_s=15.0, seed=0):
     q = x["q"].float().numpy()
     k = x["k"].float().numpy()
     v = x["v"].float().numpy()
+    k0 = x["k0"].float().numpy() if mode == 2 else None
+    v0 = x["v0"].float().numpy() if mode == 2 else None
     cores = oracle.default_threads()
     # calibrate on a small sample, then size the timed one to the budget
     n = 16 * cores
@@ -611,7 +769,7 @@ def cpu_baseline(x, scale, budget_s=15.0, seed=0):
         picks = _sample_rows(T, H, n, seed)
         rows = oracle.flat_rows(B, H, T, picks)
         t0 = time.perf_counter()
-        oracle.forward_rows(q, k, v, rows, scale=scale, nthreads=cores)
+        oracle.forward_rows(q, k, v, rows, k0, v0, scale=scale, mode=mode, nthreads=cores)
         dt = time.perf_counter() - t0
         if dt > 0.25 * budget_s or n >= 1 << 20:
             break
@@ -767,7 +925,12 @@ def main():
     ap.add_argument("--no-backward", action="store_true", help="skip the backward pass")
     ap.add_argument("--workload-steps", type=int, default=20,
                     help="timed steps of each kernel at the mid and long workloads")
-    ap.add_argument("--no-workloads", action="store_true", help="skip the mid and long workloads")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads (mid, long, tiny, stress)")
+    ap.add_argument("--shard", action="store_true",
+                    help="strong scaling: split the headline's (b, h) problems over the ranks")
+    ap.add_argument("--backend", choices=["nccl", "gloo"], default="nccl",
+                    help="process-group backend (gloo without a GPU checks the shard plan only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

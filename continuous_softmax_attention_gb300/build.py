@@ -1,6 +1,6 @@
 """Builds libcsa.so in-tree with nvcc for sm_103a.
 
-Eight translation units compiled in parallel, then linked into one shared
+Nine translation units compiled in parallel, then linked into one shared
 library next to this file.  The CUDA runtime is linked statically; the CUDA
 driver is reached at run time through the runtime's driver entry points, so
 the library loads on a machine without a GPU driver (calls then fail with
@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(HERE, "libcsa.so")
 SOURCES = ["csa_api.cu", "csa_simt.cu", "csa_tc.cu", "csa_tc_std.cu", "csa_decode.cu",
-           "csa_bwd_simt.cu", "csa_tc_bwd.cu", "csa_host.cu"]
+           "csa_bwd_simt.cu", "csa_tc_bwd.cu", "csa_host.cu", "csa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -3,6 +3,7 @@
 // host synchronisation on the compute entry points.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 
@@ -87,28 +88,48 @@ int forward_f32(const float *q, const float *k, const float *v, const float *k0,
                                           form, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int decode_bf16(const void *q, const void *k_cache, const void *v_cache, const void *k0,
-                const void *v0, const int *seqlens, void *out, float *lse, void *workspace,
-                long long workspace_bytes, int B, int H, int T, int d, float scale, int mode,
-                csa_stream_t stream) {
+// The checks of the decode step's arguments other than its workspace, in
+// csa_decode's order.  Returns CSA_OK, or the error code; *empty is set when
+// there is nothing to compute (B*H == 0).  On CSA_OK, *need holds the scratch
+// bytes the sizes take.
+int decode_check(const void *q, const void *k_cache, const void *v_cache, const void *k0,
+                 const void *v0, const int *seqlens, const void *out, const float *lse, int B,
+                 int H, int T, int d, float scale, int mode, bool *empty, long long *need) {
+    *empty = false;
     if (B < 0 || H < 0 || T < 0 || d < 1) return CSA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return CSA_ERR_INVALID_ARG;
     if (mode < CSA_K0_ZERO || mode > CSA_K0_GIVEN) return CSA_ERR_INVALID_ARG;
     if (!(d == 64 || d == 128 || d == 256)) return CSA_ERR_UNSUPPORTED;
-    if ((long long)B * H == 0) return CSA_OK;
+    if ((long long)B * H == 0) {
+        *empty = true;
+        return CSA_OK;
+    }
     if (T == 0) return CSA_ERR_INVALID_ARG;  // the newest token's own key is in the cache
-    if (!q || !k_cache || !v_cache || !out || !workspace) return CSA_ERR_INVALID_ARG;
+    if (T == INT_MAX) return CSA_ERR_UNSUPPORTED;  // positions 0..T must fit an int
+    if (!q || !k_cache || !v_cache || !out) return CSA_ERR_INVALID_ARG;
     if (mode == CSA_K0_GIVEN && (!k0 || !v0)) return CSA_ERR_INVALID_ARG;
     if ((long long)B * H * T > (1LL << 40)) return CSA_ERR_UNSUPPORTED;
-    const long long need = csa_decode_scratch_bytes(B, H, T, d);
-    if (need < 0) return CSA_ERR_UNSUPPORTED;
-    if (workspace_bytes < need) return CSA_ERR_INVALID_ARG;
+    *need = csa_decode_scratch_bytes(B, H, T, d);
+    if (*need < 0) return CSA_ERR_UNSUPPORTED;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-        !aligned(workspace, 16) || (lse && !aligned(lse, 4)) || (seqlens && !aligned(seqlens, 4)))
+        (lse && !aligned(lse, 4)) || (seqlens && !aligned(seqlens, 4)))
         return CSA_ERR_ALIGNMENT;
     if (mode == CSA_K0_GIVEN && (!aligned(k0, 16) || !aligned(v0, 16))) return CSA_ERR_ALIGNMENT;
-    int rc = device_ok();
-    if (rc != CSA_OK) return rc;
+    return CSA_OK;
+}
+
+int decode_bf16(const void *q, const void *k_cache, const void *v_cache, const void *k0,
+                const void *v0, const int *seqlens, void *out, float *lse, void *workspace,
+                long long workspace_bytes, int B, int H, int T, int d, float scale, int mode,
+                csa_stream_t stream) {
+    bool empty;
+    long long need = 0;
+    int rc = decode_check(q, k_cache, v_cache, k0, v0, seqlens, out, lse, B, H, T, d, scale, mode,
+                          &empty, &need);
+    if (rc != CSA_OK || empty) return rc;
+    if (!workspace || workspace_bytes < need) return CSA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return CSA_ERR_ALIGNMENT;
+    if ((rc = device_ok()) != CSA_OK) return rc;
     return csa_decode_run(q, k_cache, v_cache, k0, v0, seqlens, out, lse, workspace, B, H, T, d,
                           scale, mode, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -396,18 +417,18 @@ int csa_selftest_wait_timeout(unsigned timeout_us, csa_stream_t stream) {
 int csa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, const void *k0,
                        const void *v0, const int *seqlens, void *out, float *lse, int B, int H,
                        int T, int d, float scale, int k0_mode, csa_stream_t stream) {
-    const long long need = csa_decode_scratch_bytes(B, H, T, d);
+    // csa_decode's checks first, in its order; then the scratch capacity
+    bool empty;
+    long long need = 0;
+    int rc = decode_check(q, k_cache, v_cache, k0, v0, seqlens, out, lse, B, H, T, d, scale,
+                          k0_mode, &empty, &need);
+    if (rc != CSA_OK || empty) return rc;
     if (need > (long long)CSA_DECODE_NOALLOC_SCRATCH_BYTES) return CSA_ERR_UNSUPPORTED;
-    if (need < 0 || (long long)B * H == 0 || T == 0)  // answered as csa_decode answers them
-        return decode_bf16(q, k_cache, v_cache, k0, v0, seqlens, out, lse, nullptr, 0, B, H, T,
-                           d, scale, k0_mode, stream);
-    int rc = device_ok();
-    if (rc != CSA_OK) return rc;
+    if ((rc = device_ok()) != CSA_OK) return rc;
     void *scratch = nullptr;
     if ((rc = csa_decode_noalloc_scratch(&scratch)) != CSA_OK) return rc;
-    return decode_bf16(q, k_cache, v_cache, k0, v0, seqlens, out, lse, scratch,
-                       (long long)CSA_DECODE_NOALLOC_SCRATCH_BYTES, B, H, T, d, scale, k0_mode,
-                       stream);
+    return csa_decode_run(q, k_cache, v_cache, k0, v0, seqlens, out, lse, scratch, B, H, T, d,
+                          scale, k0_mode, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char *csa_status_string(int status) {

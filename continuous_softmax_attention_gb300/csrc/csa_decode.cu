@@ -491,16 +491,28 @@ int chunk_positions(int d) { return d == 64 ? DecCfg<64>::C : d == 128 ? DecCfg<
 
 }  // namespace
 
+namespace {
+// Scratch bytes for the positions [pos_lo, pos_hi) of B*H rows (positions
+// counted in 64 bits: pos_hi = T + 1 for the whole cache), or -1.
+long long range_scratch_bytes(long long B, long long H, long long pos_lo, long long pos_hi, int d) {
+    if (B < 0 || H < 0 || pos_lo < 0 || pos_hi < pos_lo || !(d == 64 || d == 128 || d == 256))
+        return -1;
+    const long long C = chunk_positions(d);
+    const long long S = (pos_hi - pos_lo + C - 1) / C;
+    // B, H < 2^31 and S < 2^31: B*H*S < 2^93 could overflow; sizes beyond
+    // 2^62 bytes are reported as unsupported (-1)
+    const long double bytes = (long double)B * H * S * (d + 2) * (long double)sizeof(float);
+    if (bytes > 4.0e18L) return -1;
+    return B * H * S * (d + 2) * (long long)sizeof(float);
+}
+}  // namespace
+
 long long csa_decode_scratch_bytes(int B, int H, int T, int d) {
-    return csa_decode_range_scratch_bytes(B, H, 0, T + 1, d);
+    return range_scratch_bytes(B, H, 0, (long long)T + 1, d);
 }
 
 long long csa_decode_range_scratch_bytes(int B, int H, int pos_lo, int pos_hi, int d) {
-    if (B < 0 || H < 0 || pos_lo < 0 || pos_hi < pos_lo || !(d == 64 || d == 128 || d == 256))
-        return -1;
-    const int C = chunk_positions(d);
-    const long long S = ((long long)pos_hi - pos_lo + C - 1) / C;
-    return (long long)B * H * S * (d + 2) * (long long)sizeof(float);
+    return range_scratch_bytes(B, H, pos_lo, pos_hi, d);
 }
 
 namespace {
@@ -566,31 +578,6 @@ int csa_decode_range_run(const void *q, const void *k_shard, const void *v_shard
                          int pos_lo, int pos_hi, cudaStream_t stream) {
     return run_range(q, k_shard, v_shard, k0, v0, seqlens, nullptr, out, lse, scratch, B, H, T, d,
                      scale, mode, pos_lo, pos_hi, stream);
-}
-
-// Scratch of csa_decode_noalloc: a file-scope device array, so that the
-// entry point allocates nothing.  Its address is looked up once per device.
-static __device__ __align__(256) float g_noalloc_scratch[CSA_DECODE_NOALLOC_SCRATCH_BYTES / 4];
-
-namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mutex;
-void *g_noalloc_addr[kMaxDevices];
-}  // namespace
-
-int csa_decode_noalloc_scratch(void **addr) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return CSA_ERR_NO_DEVICE;
-    if (dev < 0 || dev >= kMaxDevices) return CSA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_addr[dev]) {
-        void *p = nullptr;
-        // dev is the current device here, so the address is that device's copy.
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return CSA_ERR_CUDA;
-        g_noalloc_addr[dev] = p;
-    }
-    *addr = g_noalloc_addr[dev];
-    return CSA_OK;
 }
 
 int csa_decode_take_status(void) {

@@ -313,15 +313,24 @@ int csa_decode(const void *q, const void *k_cache, const void *v_cache, const vo
  * csa_decode_noalloc - csa_decode without a caller workspace.  The method's
  *   pages have no counterpart to this entry point: it is a convenience of
  *   this library for callers that cannot hand over scratch memory.
- *   Same arguments, result, validation and error codes as csa_decode, minus
- *   workspace and workspace_bytes.  The chunk partials go to a fixed scratch
- *   array of CSA_DECODE_NOALLOC_SCRATCH_BYTES bytes that lives in the
- *   library's device image (one per device); the call allocates no memory of
- *   any kind.  Sizes whose csa_decode_workspace_bytes exceeds that capacity
- *   are rejected with CSA_ERR_UNSUPPORTED before anything is launched.
- *   The first call on each device looks the scratch address up with
- *   cudaGetSymbolAddress (that device must be current): make that first call
+ *   Same arguments and result as csa_decode, minus workspace and
+ *   workspace_bytes.  The chunk partials go to a fixed scratch array of
+ *   CSA_DECODE_NOALLOC_SCRATCH_BYTES bytes that lives in the library's device
+ *   image (one per device); the call allocates no memory of any kind.  Each
+ *   call writes every partial it reads, so nothing in the array needs to
+ *   start at zero.
+ *   Memory: the array is CSA_DECODE_NOALLOC_SCRATCH_BYTES (64 MiB) of device
+ *   memory on each device that loads it, held until the process exits.  It
+ *   sits in a module of its own: with lazy module loading (the CUDA
+ *   default) only processes that call csa_decode_noalloc hold it.
+ *   Set-up: the first call on a device, and the first call after a device
+ *   reset (a new context), looks the scratch address up with
+ *   cudaGetSymbolAddress (that device must be current): make that call
  *   before any stream capture begins.
+ *   Checks: csa_decode's argument checks run first, in its order and with
+ *   its error codes; a size that passes them but whose scratch need exceeds
+ *   the capacity then gives CSA_ERR_UNSUPPORTED, before anything is
+ *   launched.
  *   Concurrency: every call on a device shares that one scratch array, so
  *   calls that can overlap on the device (different streams, or several host
  *   threads) race and corrupt each other's results.  Serialise them, e.g. on
@@ -334,8 +343,8 @@ int csa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, 
 
 /*
  * csa_decode_workspace_bytes - bytes of workspace csa_decode needs for these
- *   sizes (host only, no device needed), or -1 for a negative size or a d
- *   other than 64, 128, 256.
+ *   sizes (host only, no device needed), or -1 for a negative size, a d
+ *   other than 64, 128, 256, or a size beyond 2^62 bytes.
  */
 long long csa_decode_workspace_bytes(int B, int H, int T, int d);
 

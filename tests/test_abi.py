@@ -109,6 +109,10 @@ def test_decode_workspace_bytes(lib):
     assert lib.csa_decode_workspace_bytes(0, 5, 10, 64) == 0
     assert lib.csa_decode_workspace_bytes(1, 1, 10, 96) == -1
     assert lib.csa_decode_workspace_bytes(1, -1, 10, 64) == -1
+    # positions 0..T counted in 64 bits: no overflow at the largest T
+    imax = 2 ** 31 - 1
+    assert lib.csa_decode_workspace_bytes(1, 1, imax, 128) == ((imax + 1 + 125) // 126) * 130 * 4
+    assert lib.csa_decode_workspace_bytes(imax, imax, imax, 256) == -1  # beyond 2^62 bytes
 
 
 def test_decode_validation(lib):
@@ -120,6 +124,7 @@ def test_decode_validation(lib):
     assert dec(lib, mode=-1) == L.CSA_ERR_INVALID_ARG
     assert dec(lib, scale=float("nan")) == L.CSA_ERR_INVALID_ARG
     assert dec(lib, T=0) == L.CSA_ERR_INVALID_ARG  # a query needs its own key
+    assert dec(lib, B=1, H=1, T=2 ** 31 - 1) == L.CSA_ERR_UNSUPPORTED  # positions 0..T
     assert dec(lib, d=96) == L.CSA_ERR_UNSUPPORTED
     assert dec(lib, d=0) == L.CSA_ERR_INVALID_ARG
     assert dec(lib, k=ctypes.c_void_p(4104)) == L.CSA_ERR_ALIGNMENT

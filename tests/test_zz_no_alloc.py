@@ -44,9 +44,12 @@ def test_noalloc_equals_workspace_entry_point_twice(d, mode):
         out = torch.full_like(ref_o, float("nan"))
         lse = torch.full_like(ref_l, float("nan"))
         free_before = torch.cuda.mem_get_info()[0]
+        alloc_before = torch.cuda.memory_allocated()
         rc = _noalloc(lib, g, out, lse, B, H, T, d, scale, mode)
         torch.cuda.synchronize()
         assert rc == 0, L.status_string(rc)
+        # nothing taken from torch's caching allocator, on any call
+        assert torch.cuda.memory_allocated() == alloc_before
         if call == 1:  # scratch set up by now: the call must not take device memory
             assert torch.cuda.mem_get_info()[0] == free_before
         assert torch.equal(out, ref_o), f"call {call}: outputs differ"
@@ -68,6 +71,48 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     out = torch.empty(1, 1, d, dtype=torch.bfloat16, device="cuda")
     assert _noalloc(lib, g, out, None, 1, 1, 300, d, 0.1, 0) == 0
     torch.cuda.synchronize()
+
+
+def test_noalloc_at_and_just_past_its_capacity():
+    """The largest size that fits the scratch (B*H*S*(d+2)*4 bytes, S the
+    chunks of a row: 2^26 is not reachable, 264 bytes short is) runs and
+    matches csa_decode bit for bit; one more head does not fit and is
+    rejected before any launch."""
+    lib = _bind(L.load())
+    d, T, B = 128, 1, 1
+    H_fit = SCRATCH_BYTES // ((d + 2) * 4)  # one chunk per row at T = 1
+    assert decode_workspace_bytes(B, H_fit, T, d) <= SCRATCH_BYTES
+    assert decode_workspace_bytes(B, H_fit + 1, T, d) > SCRATCH_BYTES
+    x = make_decode_inputs(B, H_fit, T, d, seed=7, len_lo=1)
+    g = {k: t.cuda() for k, t in x.items()}
+    ref_o, ref_l = decode(g["q"], g["k"], g["v"], seqlens=g["seqlens"], scale=0.1)
+    out = torch.full_like(ref_o, float("nan"))
+    lse = torch.full_like(ref_l, float("nan"))
+    rc = _noalloc(lib, g, out, lse, B, H_fit, T, d, 0.1, 0)
+    torch.cuda.synchronize()
+    assert rc == 0, L.status_string(rc)
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: rejected before any launch
+    rc = lib.csa_decode_noalloc(fake, fake, fake, None, None, None, fake, None, B, H_fit + 1, T, d,
+                                ctypes.c_float(0.1), 0, None)
+    assert rc == L.CSA_ERR_UNSUPPORTED
+
+
+def test_noalloc_checks_arguments_before_its_capacity():
+    """An oversized call with a bad argument gets csa_decode's error for that
+    argument, not the capacity's."""
+    lib = _bind(L.load())
+    fake = ctypes.c_void_p(1 << 20)
+    B, H, T, d = 64, 64, 16384, 128
+    assert decode_workspace_bytes(B, H, T, d) > SCRATCH_BYTES
+    call = lambda q=fake, mode=0, scale=0.1: lib.csa_decode_noalloc(
+        q, fake, fake, None, None, None, fake, None, B, H, T, d, ctypes.c_float(scale), mode, None)
+    assert call() == L.CSA_ERR_UNSUPPORTED
+    assert call(q=None) == L.CSA_ERR_INVALID_ARG
+    assert call(mode=7) == L.CSA_ERR_INVALID_ARG
+    assert call(mode=2) == L.CSA_ERR_INVALID_ARG  # given sink without k0, v0
+    assert call(scale=float("inf")) == L.CSA_ERR_INVALID_ARG
+    assert call(q=ctypes.c_void_p((1 << 20) + 2)) == L.CSA_ERR_ALIGNMENT
 
 
 def test_noalloc_argument_errors_match_decode():
