@@ -139,7 +139,13 @@ struct TcCfg {
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     // the epilogue's exchange: [2 halves][128 rows][4] (max, sum, sink weight)
     static constexpr int kOffXFin = kOffMisc + 64;
-    static constexpr int kSmemBytes = kOffXFin + 2 * 128 * 4 * 4 + 1024;  // + slack to align the base
+    // d = 128: the output rows of each softmax warp (32 rows x 64 columns,
+    // bf16, 128B-swizzled) staged for one TMA store per item
+    static constexpr bool kTmaOut = D == 128;
+    static constexpr int kOffOut = (kOffXFin + 2 * 128 * 4 * 4 + 1023) / 1024 * 1024;
+    static constexpr int kOutBytes = kTmaOut ? 8 * 32 * 128 : 0;
+    static constexpr int kSmemBytes = kOffOut + kOutBytes + 1024;  // + slack to align the base
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
     // TMEM columns: S buffer 0 | S buffer 1 | O_0 | O_1
     __device__ static constexpr uint32_t col_s(int b) { return (uint32_t)(kNK * b); }
     __device__ static constexpr uint32_t col_o(int h) { return (uint32_t)(2 * kNK + kN * h); }
@@ -286,6 +292,36 @@ inline bool encode_rows_map(CUtensorMap *map, const void *ptr, int BH, int T, in
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return rc == CUDA_SUCCESS;
 }
+
+// The output viewed as the same 3-D tensor {D, T, B*H}, with boxes of 64
+// columns x 32 rows (one softmax warp's rows of one column half); rows past
+// T are not written.
+inline bool encode_out_map(CUtensorMap *map, void *ptr, int BH, int T, int D) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
+    const cuuint32_t box[3] = {64, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult rc = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return rc == CUDA_SUCCESS;
+}
+
+// 3-D tiled TMA store of one box from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const void *desc, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 ::"l"(reinterpret_cast<uint64_t>(desc)), "r"(c0), "r"(c1), "r"(c2), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of this thread's committed stores have been read
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// this thread's committed stores have completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ------------------------------------------------------------- weights
 // One interval's two end weights, times (ln 2)^2.  X = u_right - u_left in
@@ -508,29 +544,80 @@ __device__ __forceinline__ void short_chunk(const float (&s)[NCK + 1], const Row
 
 // Max of the valid scaled logits a*log2(e) of one half-row in the query
 // tile's first key tile: the half's columns and the neighbour column its
-// intervals reach (columns c0..c0+h0, c0 = h (h0 - 1)).  Column 0 is no
-// position there, column 1 is the sink (none in SYM).  -inf if the half
-// holds none of the row's keys; it then holds none of them in any later
-// tile either.
-template <bool SYM>
-__device__ __forceinline__ float first_tile_max(uint32_t tS, const RowState &st, int c0, int h0,
+// intervals reach (columns c0..c0+h0, c0 = h (h0 - 1)), read in one batch
+// of TMEM loads.  Column 0 is no position there, column 1 is the sink (none
+// in SYM).  -inf if the half holds none of the row's keys; it then holds
+// none of them in any later tile either.
+__device__ __forceinline__ float fmin3f(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+template <int H0, bool SYM>
+__device__ __forceinline__ float first_tile_max(uint32_t tS, const RowState &st, int c0,
                                                 int c_last) {
-    float m = -INFINITY;
-#pragma unroll 1
-    for (int o = 0; o <= h0; o += 8) {
-        uint32_t t[8];
-        tmem_ld8(tS + c0 + o, t);
-        tmem_wait_ld8(t);
+    static_assert(H0 == 56 || H0 == 64, "column halves of 56 or 64 keys");
+    uint32_t a[32], b[H0 == 64 ? 32 : 16], e8[8], z[1];
+    tmem_ld32(tS + c0, a);
+    if constexpr (H0 == 64) {
+        tmem_ld32(tS + c0 + 32, b);
+    } else {
+        tmem_ld16(tS + c0 + 32, b);
+        tmem_ld8(tS + c0 + 48, e8);
+    }
+    tmem_ld1(tS + c0 + H0, z[0]);
+    tmem_wait_ld_regs<32>(a);
+    if constexpr (H0 == 64) {
+        tmem_wait_ld_regs<32>(b);
+    } else {
+        tmem_wait_ld16(b);
+        tmem_wait_ld8(e8);
+    }
+    tmem_wait_ld_regs<1>(z);
+    auto val = [&](int i) {
+        return __uint_as_float(i < 32 ? a[i & 31]
+                                      : (i == H0 ? z[0]
+                                                 : (H0 == 64 || i < 48 ? b[(i - 32) & 31]
+                                                                       : e8[(i - 48) & 7])));
+    };
+    if (H0 == 56 && c_last >= c0 + H0) {
+        // every column of the window from column 2 on is one of the row's
+        // keys: the max (scale < 0: the min) of the raw logits, scaled once
+        float hi, lo;
+        auto scan = [&](auto first) {
+            // columns first .. H0 in pairs (the last pair may repeat one)
+            constexpr int F = decltype(first)::value;
+            hi = lo = val(F);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int col = c0 + o + i;
-            float v = __uint_as_float(t[i]);
-            if (col == 1 && st.mode == CSA_K0_GIVEN) v = st.s_sink;
-            // the copied sink duplicates column 2
-            const bool skip = col == 0 || (col == 1 && (SYM || st.mode == CSA_K0_COPY_FIRST)) ||
-                              o + i > h0;
-            m = !skip && col <= c_last ? fmaxf(m, v * st.k2) : m;
+            for (int i = F + 1; i <= H0; i += 2) {
+                const float x = val(i), y = val(i + 1 <= H0 ? i + 1 : i);
+                hi = fmax3f(hi, x, y);
+                lo = fmin3f(lo, x, y);
+            }
+        };
+        if (c0 == 0)
+            scan(std::integral_constant<int, 2>{});
+        else
+            scan(std::integral_constant<int, 0>{});
+        if (c0 == 0) {
+            // column 1: the sink, a key unless copied (or no sink at all)
+            const float v1 = st.mode == CSA_K0_GIVEN ? st.s_sink : val(1);
+            const bool in = !SYM && st.mode != CSA_K0_COPY_FIRST;
+            hi = in ? fmaxf(hi, v1) : hi;
+            lo = in ? fminf(lo, v1) : lo;
         }
+        return st.k2 >= 0.0f ? hi * st.k2 : lo * st.k2;
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i <= H0; ++i) {
+        const int col = c0 + i;
+        float v = val(i);
+        if (col == 1 && st.mode == CSA_K0_GIVEN) v = st.s_sink;
+        // the copied sink duplicates column 2
+        const bool skip = col == 0 || (col == 1 && (SYM || st.mode == CSA_K0_COPY_FIRST));
+        m = !skip && col <= c_last ? fmaxf(m, v * st.k2) : m;
     }
     return m;
 }
@@ -712,7 +799,8 @@ template <int D, bool SHORT, bool SYM>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_forward_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_o, const TcParams p) {
     using C = TcCfg<D>;
     constexpr int NSK = C::kStagesK, NSV = C::kStagesV;
     constexpr int KS = C::kKS;
@@ -797,6 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
+            if (C::kTmaOut) tma_prefetch_desc(&tm_o);
             int item = (int)blockIdx.x;
             int issued_q = 0, issued_k = 0, issued_v = 0;  // loads issued (K, V: tiles)
             bool ok = true;
@@ -990,7 +1079,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // last valid column of this row, and whether the tile needs masks
                 const int c_last = r + 2 - KS * j;
                 const bool masked = KS * (j + 1) > row0 + 1;
-                if (j == 0) st.m = first_tile_max<SYM>(tS, st, h * (C::kH0 - 1), C::kH0, c_last);
+                if (j == 0) st.m = first_tile_max<C::kH0, SYM>(tS, st, h * (C::kH0 - 1), c_last);
                 const uint32_t odone = BAR(C::kBarODone), par = (g - 1) & 1;
                 ok = masked ? half_tile<D, SHORT, SYM, true>(tS, tO, st, h, c_last, j == 0, j > 0,
                                                              odone, par, abort_flag)
@@ -1032,10 +1121,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld_regs<1>(rs[1]);
             const float den = fmaf(a0, __uint_as_float(rs[0][0]) + w_sink, a1 * __uint_as_float(rs[1][0]));
             const float inv_l = 1.0f / den;
+            const float c0 = a0 * inv_l, c1 = a1 * inv_l;
             const bool store = r < T;
             __nv_bfloat16 *orow =
                 p.out + ((size_t)bh * T + (size_t)(store ? r : 0)) * D + h * (D / 2);
             const __nv_bfloat16 *v0h = p.v0 + (size_t)(bh % p.H) * D + h * (D / 2);
+            uint8_t *stage = smem + C::kOffOut + warp * 4096;
+            if (C::kTmaOut) {
+                // the previous item's store from this warp's stage has read it
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+            }
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t o0[32], o1[32];
@@ -1054,11 +1150,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(val[2 * e], val[2 * e + 1]);
-                if (store) {
+                if (C::kTmaOut) {
+                    // this row's 16-byte chunks 4 cc .. 4 cc + 3 of the staged box
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        *reinterpret_cast<uint4 *>(stage + lane * 128 + (((4 * cc + e) ^ (lane & 7)) << 4)) =
+                            make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                } else if (store) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * cc);
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                }
+            }
+            if (C::kTmaOut) {
+                // one TMA store of the warp's 32 rows x 64 columns (rows past T
+                // are not written; a box wholly past T is not issued)
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && row0 + 32 * wq < T) {
+                    tma_store_3d(&tm_o, smem_u32(stage), h * (D / 2), row0 + 32 * wq, bh);
+                    bulk_commit();
                 }
             }
             if (store && h == 0 && p.lse)
@@ -1066,6 +1178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     (mx + log2f(fmaf(a0, l0, a1 * l1))) * kLn2 + (SHORT ? 0.0f : kLseShift);
             tc_fence_before();
         }
+        // the output stores are complete before the block exits
+        if (C::kTmaOut && lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -1157,9 +1271,9 @@ int launch_tc(const void *q, const void *k, const void *v, const void *k0, const
               cudaStream_t stream) {
     using C = TcCfg<D>;
     const int BH = B * H;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!encode_qkv_map(&mq, q, BH, T, D) || !encode_rows_map(&mk, k, BH, T, D, C::kNK) ||
-        !encode_rows_map(&mv, v, BH, T, D, C::kNK))
+        !encode_rows_map(&mv, v, BH, T, D, C::kNK) || !encode_out_map(&mo, out, BH, T, D))
         return CSA_ERR_CUDA;
     TcParams prm;
     prm.B = B;
@@ -1187,7 +1301,7 @@ int launch_tc(const void *q, const void *k, const void *v, const void *k0, const
         return CSA_ERR_CUDA;
     return launch_with_slot(dev, stream, [&](int slot) {
         prm.slot = slot;
-        kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, prm);
+        kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, prm);
         return cudaGetLastError() == cudaSuccess;
     });
 }
