@@ -151,7 +151,8 @@ struct BwCfg {
     // (where dS was, at d = 128)
     static constexpr int kBarStageFull = kBarPFree + 1;     // [2], one per column half
     static constexpr int kBarStageFree = kBarStageFull + 2; // its reductions have read it
-    static constexpr int kBarDrain = kBarStageFree + 1;
+    static constexpr int kBarSEarly = kBarStageFree + 1;    // S(j+1) in TMEM (before dP(j+1))
+    static constexpr int kBarDrain = kBarSEarly + 1;
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
@@ -298,6 +299,67 @@ __device__ __forceinline__ void cols16(const float (&sv)[17], const float (&gv)[
     }
 }
 
+// cols16 in two parts.  The first needs only the logits: P (masked) and
+// the flux coefficient k of each column's right interval (zero where that
+// interval does not exist), carrying the L share Lc across chunks.  The
+// second adds dP: the fluxes F and dS, carrying Fc; it also packs P and dS.
+template <bool MASKED>
+__device__ __forceinline__ void cols16_s(const float (&sv)[17], float k2, float lse2, int c0,
+                                         int c_last, bool last_chunk, float &Lc, float (&Pv)[16],
+                                         float (&kv)[16]) {
+    float u[17], pe[17];
+#pragma unroll
+    for (int i = 0; i < 17; ++i) {
+        u[i] = fmaf(sv[i], k2, -lse2);
+        pe[i] = ex2_approx(u[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int c = c0 + i;
+        float R, Ln, kf;
+        interval(u[i], u[i + 1], pe[i], pe[i + 1], R, Ln, kf);
+        bool seg = true, key = true;
+        if (MASKED) {
+            seg = c + 1 <= c_last;
+            key = c <= c_last;
+        }
+        if (i == 15) seg = seg && !last_chunk;
+        if (MASKED || i == 15) {
+            R = seg ? R : 0.0f;
+            Ln = seg ? Ln : 0.0f;
+            kf = seg ? kf : 0.0f;
+        }
+        float P = Lc + R;
+        if (MASKED) P = key ? P : 0.0f;
+        Pv[i] = P;
+        kv[i] = kf;
+        Lc = Ln;
+    }
+}
+
+template <bool MASKED>
+__device__ __forceinline__ void cols16_d(const float (&gv)[17], const float (&Pv)[16],
+                                         const float (&kv)[16], float Dr, float scale, int c0,
+                                         int c_last, bool zero_c0, bool last_chunk, float &Fc,
+                                         uint32_t (&pP)[8], uint32_t (&pS)[8]) {
+    float Sv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float Fn = kv[i] * (gv[i] - gv[i + 1]);
+        float ds = scale * fmaf(Pv[i], gv[i] - Dr, Fc - Fn);
+        if (MASKED) ds = c0 + i <= c_last ? ds : 0.0f;
+        if (i == 0 && zero_c0) ds = 0.0f;
+        if (i == 15 && last_chunk) ds = 0.0f;
+        Sv[i] = ds;
+        Fc = Fn;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        pP[i] = pack_bf16x2(Pv[2 * i], Pv[2 * i + 1]);
+        pS[i] = pack_bf16x2(Sv[2 * i], Sv[2 * i + 1]);
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_backward_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -351,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(BAR(C::kBarStageFull), 128);
         mbar_init(BAR(C::kBarStageFull + 1), 128);
         mbar_init(BAR(C::kBarStageFree), 1);
+        mbar_init(BAR(C::kBarSEarly), 1);
         mbar_init(BAR(C::kBarDrain), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -478,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = wait_b(BAR(C::kBarQFull + sq1), ((j + 1) / NQ) & 1, abort_flag))) break;
                     tc_fence_after();
                     issue_s(sQ + sq1 * C::kTileBytes);
+                    tc_commit(BAR(C::kBarSEarly));
                 }
                 if (!(ok = wait_b(BAR(C::kBarPReady), j & 1, abort_flag))) break;
                 tc_fence_after();
@@ -549,6 +613,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         int r_next = 128 * q_first + irow;
         float lse_next = r_next < T ? p.lse[(size_t)bh * T + r_next] : 0.0f;
         float D_next = r_next < T ? p.Drow[(size_t)bh * T + r_next] : 0.0f;
+        const int cb = 64 * half;
+        // Chunk 0 (this half's first 16 columns) of a query tile, from S alone:
+        // P, the flux coefficients of its intervals, the L share carried into
+        // chunk 1 and, for half 1, the coefficient of the interval (63, 64)
+        // entering it.  Computed during the previous tile's wait for its dV
+        // and dQ_part products (S of this tile is in TMEM by then), or at the
+        // start of the first tile.
+        float P0[16], k0v[16], Lc1 = 0.0f, k63 = 0.0f;
+        bool pre = false;
+        auto chunk0_s = [&](float lse2c, int c_lastc, bool maskedc) {
+            uint32_t a0[16], an0 = 0u, e0 = 0u, e1 = 0u;
+            tmem_ld16(tS + cb, a0);
+            tmem_ld1(tS + cb + 16, an0);
+            if (half == 1) {
+                tmem_ld1(tS + 63, e0);
+                tmem_ld1(tS + 64, e1);
+            }
+            wait_ld17(a0, an0);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(e0), "+r"(e1) : : "memory");
+            float Lc = 0.0f;
+            k63 = 0.0f;
+            if (half == 1) {
+                const float u0 = fmaf(__uint_as_float(e0), k2, -lse2c);
+                const float u1 = fmaf(__uint_as_float(e1), k2, -lse2c);
+                float R, L, kf;
+                interval(u0, u1, ex2_approx(u0), ex2_approx(u1), R, L, kf);
+                const bool seg = 64 <= c_lastc;
+                Lc = seg ? L : 0.0f;
+                k63 = seg ? kf : 0.0f;
+            }
+            float sv[17];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sv[i] = __uint_as_float(a0[i]);
+            sv[16] = __uint_as_float(an0);
+            if (maskedc)
+                cols16_s<true>(sv, k2, lse2c, cb, c_lastc, false, Lc, P0, k0v);
+            else
+                cols16_s<false>(sv, k2, lse2c, cb, c_lastc, false, Lc, P0, k0v);
+            Lc1 = Lc;
+        };
+        // last column of tile j that a row sees (its own key, position r + 1),
+        // and whether the tile needs masks (some row stops before column 127)
+        auto tile_clast = [&](int r) { return r < T ? min(r + 1 - kKeyStride * kt, 127) : -1; };
+        auto tile_masked = [&](int row0) {
+            return row0 + 1 - kKeyStride * kt < 127 || row0 + 127 >= T;
+        };
         for (int j = 0; ok && j < nQ; ++j) {
             const int row0 = 128 * (q_first + j);
             const int r = row0 + irow;  // query row
@@ -560,38 +670,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lse_next = p.lse[(size_t)bh * T + r_next];
                 D_next = p.Drow[(size_t)bh * T + r_next];
             }
-            // last column of the tile this row sees (its own key, position r + 1)
-            const int c_last = rvalid ? min(r + 1 - kKeyStride * kt, 127) : -1;
-            // the tile needs masks if some row of it stops before column 127
-            const bool masked = row0 + 1 - kKeyStride * kt < 127 || row0 + 127 >= T;
+            const int c_last = tile_clast(r);
+            const bool masked = tile_masked(row0);
             ok = __all_sync(0xffffffffu, wait_b(BAR(C::kBarSFull), j & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            // L share and flux entering this half's first column from the left
-            float Lc = 0.0f, Fc = 0.0f;
-            if (half == 1) {
-                uint32_t e[4];
-                tmem_ld1(tS + 63, e[0]);
-                tmem_ld1(tS + 64, e[1]);
-                tmem_ld1(tD + 63, e[2]);
-                tmem_ld1(tD + 64, e[3]);
-                asm volatile("tcgen05.wait::ld.sync.aligned;"
-                             : "+r"(e[0]), "+r"(e[1]), "+r"(e[2]), "+r"(e[3])
-                             :
-                             : "memory");
-                const float u0 = fmaf(__uint_as_float(e[0]), k2, -lse2);
-                const float u1 = fmaf(__uint_as_float(e[1]), k2, -lse2);
-                float R, L, kf;
-                interval(u0, u1, ex2_approx(u0), ex2_approx(u1), R, L, kf);
-                const bool seg = 64 <= c_last;
-                Lc = seg ? L : 0.0f;
-                Fc = seg ? kf * (__uint_as_float(e[2]) - __uint_as_float(e[3])) : 0.0f;
-            }
-            // four chunks of 16 columns; the TMEM loads of chunk kk+1 are in
-            // flight while chunk kk is computed
-            uint32_t a[16], g[16], an[1] = {0u}, gn[1] = {0u};
-            const int cb = 64 * half;
-            uint32_t hP[8], hS[8];  // chunk 0's P and dS while they are held (d = 128)
+            if (!pre) chunk0_s(lse2, c_last, masked);
+            pre = false;
             // this row's 16 keys from column c0 = 16-byte chunks ch, ch+1 of box c0/64
             auto store_pds = [&](int c0, const uint32_t (&qP)[8], const uint32_t (&qS)[8]) {
                 const int box = c0 >> 6, ch = (c0 & 63) >> 3;
@@ -606,12 +691,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                         make_uint4(qS[4 * h2], qS[4 * h2 + 1], qS[4 * h2 + 2], qS[4 * h2 + 3]);
                 }
             };
-            tmem_ld16(tS + cb, a);
-            tmem_ld16(tD + cb, g);
-            tmem_ld1(tS + cb + 16, an[0]);
-            tmem_ld1(tD + cb + 16, gn[0]);
+            // dP of chunk 0 (and of half 1's entering interval); S and dP of
+            // chunk 1, in flight while chunk 0 is finished
+            uint32_t a[16], g[16], an[1] = {0u}, gn[1] = {0u};
+            uint32_t g0[16], g0n = 0u, d0 = 0u, d1 = 0u;
+            tmem_ld16(tD + cb, g0);
+            tmem_ld1(tD + cb + 16, g0n);
+            if (half == 1) {
+                tmem_ld1(tD + 63, d0);
+                tmem_ld1(tD + 64, d1);
+            }
+            wait_ld17(g0, g0n);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(d0), "+r"(d1) : : "memory");
+            tmem_ld16(tS + cb + 16, a);
+            tmem_ld16(tD + cb + 16, g);
+            tmem_ld1(tS + cb + 32, an[0]);
+            tmem_ld1(tD + cb + 32, gn[0]);
+            float Lc = Lc1;
+            float Fc = half == 1 ? k63 * (__uint_as_float(d0) - __uint_as_float(d1)) : 0.0f;
+            uint32_t hP[8], hS[8];  // chunk 0's P and dS
+            {
+                float gv[17];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) gv[i] = __uint_as_float(g0[i]);
+                gv[16] = __uint_as_float(g0n);
+                const bool zero_c0 = cb == 0 && kt > 0;
+                if (masked)
+                    cols16_d<true>(gv, P0, k0v, Dr, scale, cb, c_last, zero_c0, false, Fc, hP, hS);
+                else
+                    cols16_d<false>(gv, P0, k0v, Dr, scale, cb, c_last, zero_c0, false, Fc, hP, hS);
+            }
+            // P and dS overwrite the previous tile's staged dQ_part: wait until
+            // its reductions have read it (the MMAs reading the previous P
+            // and dS finished before this tile's S and dP did).  At d = 128,
+            // where those reductions take longest, chunk 0's P and dS are held
+            // in registers and stored after chunk 1, so the wait comes later.
+            constexpr int kFirstStore = D == 128 ? 1 : 0;
+            if (kFirstStore == 0) {
+                if (j > 0 &&
+                    !__all_sync(0xffffffffu, wait_b(BAR(C::kBarStageFree), (j - 1) & 1, abort_flag))) {
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");  // chunk 1's loads
+                    ok = false;
+                    break;
+                }
+                store_pds(cb, hP, hS);
+            }
 #pragma unroll 1
-            for (int kk = 0; kk < 4; ++kk) {
+            for (int kk = 1; kk < 4; ++kk) {
                 const int c0 = cb + 16 * kk;
                 wait_ld17(a, an[0]);
                 wait_ld17(g, gn[0]);
@@ -635,41 +761,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld1(tD + c0 + 32, gn[0]);
                     }
                 }
-                const bool zero_c0 = c0 == 0 && kt > 0, last_chunk = c0 == 112;
+                const bool last_chunk = c0 == 112;
                 uint32_t pP[8], pS[8];
                 if (masked)
-                    cols16<true>(sv, gv, k2, lse2, Dr, scale, c0, c_last, zero_c0, last_chunk, Lc,
+                    cols16<true>(sv, gv, k2, lse2, Dr, scale, c0, c_last, false, last_chunk, Lc,
                                  Fc, pP, pS);
                 else
-                    cols16<false>(sv, gv, k2, lse2, Dr, scale, c0, c_last, zero_c0, last_chunk,
+                    cols16<false>(sv, gv, k2, lse2, Dr, scale, c0, c_last, false, last_chunk,
                                   Lc, Fc, pP, pS);
-                // P and dS overwrite the previous tile's staged dQ_part: wait until
-                // its reductions have read it (the MMAs reading the previous P
-                // and dS finished before this tile's S and dP did).  At d = 128,
-                // where those reductions take longest, chunk 0's P and dS are held
-                // in registers and stored after chunk 1, so the wait comes later.
-                constexpr int kFirstStore = D == 128 ? 1 : 0;
-                if (kFirstStore == 1 && kk == 0) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        hP[i] = pP[i];
-                        hS[i] = pS[i];
+                if (kFirstStore == 1 && kk == 1) {
+                    if (j > 0 &&
+                        !__all_sync(0xffffffffu, wait_b(BAR(C::kBarStageFree), (j - 1) & 1, abort_flag))) {
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");  // the next chunk's loads
+                        ok = false;
+                        break;
                     }
-                    continue;
+                    store_pds(cb, hP, hS);
                 }
-                if (kk == kFirstStore && j > 0 &&
-                    !__all_sync(0xffffffffu, wait_b(BAR(C::kBarStageFree), (j - 1) & 1, abort_flag))) {
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");  // the next chunk's loads
-                    ok = false;
-                    break;
-                }
-                if (kFirstStore == 1 && kk == 1) store_pds(cb, hP, hS);
                 store_pds(c0, pP, pS);
             }
             if (!ok) break;
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(BAR(C::kBarPReady));
+            // the next tile's chunk 0 from its S while dV and dQ_part run
+            if (D == 128 && j + 1 < nQ) {
+                ok = __all_sync(0xffffffffu, wait_b(BAR(C::kBarSEarly), j & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                const int r1 = r + 128;
+                chunk0_s(r1 < T ? lse_next * kLog2e : 0.0f, tile_clast(r1), tile_masked(row0 + 128));
+                pre = true;
+            }
             // dQ_part of this query tile (in the dP columns): out of TMEM, which
             // frees the dP columns, then staged in fp32 where P and dS were, as
             // 128B-swizzled boxes of [128 rows][32 columns] for the reducer
