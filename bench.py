@@ -15,6 +15,10 @@ Also reported on the same JSON line:
                through two alternating workspaces, across consecutive steps
   std          the library's standard causal attention kernel (eq. (12)) at
                the same shape, and the ratio continuous / standard
+  short_conv, symmetric, log_domain
+               the other forms of the same step: the first-order reading of
+               eq. (13), the symmetric interval, and the interval weights
+               formed in the log domain (the reference evaluation)
   roofline     tensor-core bound: algorithmic matmul flops / kernel time
                against the measured dense bf16 peak
   cpu_baseline the CPU oracle (double precision, all host cores) on a
@@ -280,6 +284,8 @@ def run_gpu(args):
     sc_call = lambda: csa.forward(g["q"], g["k"], g["v"], mode=w.modes[0], scale=scale, out=out,
                                   lse=lse, short_conv=True)
     sym_call = lambda: csa.forward_symmetric(g["q"], g["k"], g["v"], scale=scale, out=out, lse=lse)
+    ld_call = lambda: csa.forward(g["q"], g["k"], g["v"], mode=w.modes[0], scale=scale, out=out,
+                                  lse=lse, log_domain=True)
     std_call = lambda: csa.std_forward(g["q"], g["k"], g["v"], scale=scale, out=out, lse=lse)
 
     dec = None if args.no_decode else DecodeBench(csa, dev, stream, flush)
@@ -320,6 +326,7 @@ def run_gpu(args):
         std_call()
         sc_call()
         sym_call()
+        ld_call()
         e2e_call()
         if dec is not None:
             dec.call()
@@ -338,6 +345,7 @@ def run_gpu(args):
         ms_std = timed(std_call, args.steps)
         ms_sc = timed(sc_call, args.steps)
         ms_sym = timed(sym_call, args.steps)
+        ms_ld = timed(ld_call, args.steps)
         ms_e2e = timed_region(e2e_call, args.steps)
         if dec is not None:
             dec.ms = timed(dec.call, args.decode_steps)
@@ -356,6 +364,7 @@ def run_gpu(args):
     tot_csa, tot_std, tot_e2e = total(ms_csa), total(ms_std), total(ms_e2e)
     tot_sc = total(ms_sc)
     tot_sym = total(ms_sym)
+    tot_ld = total(ms_ld)
     # every rank takes part in the max over ranks of every leg before the
     # process group goes away
     if dec is not None:
@@ -416,7 +425,11 @@ def run_gpu(args):
                       "unit": UNIT, "ms_per_step": round(tot_sym / K, 5),
                       "note": "eq. (2) over [1/2, t+1/2] (csa_forward_symmetric); flops over its "
                               "B*H*T(T+1)/2 pairs (no sink)"},
-        "gpu_launches": 4 * K + K * (B * H // e2e_hpc) +
+        "log_domain": {"value": round(rep_world * flops * K / (tot_ld * 1e-3) / 1e12, 3), "unit": UNIT,
+                       "ms_per_step": round(tot_ld / K, 5),
+                       "note": "the same step with z = a + b formed in the log domain "
+                               "(csa_forward_logdomain), the reference evaluation of the weights"},
+        "gpu_launches": 5 * K + K * (B * H // e2e_hpc) +
                         (0 if dec is None else 2 * 2 * args.decode_steps) +
                         (0 if bwd is None else bwd.launches * args.backward_steps) +
                         (0 if more is None else more.launches * args.workload_steps),

@@ -50,6 +50,7 @@ def load():
     bwd = [p, p, p, p, p, p, p, p, p, p, p, p, p, p, ctypes.c_longlong, i, i, i, i, f, i, p]
     for name, args in (("csa_forward", fwd), ("csa_forward_f32", fwd),
                        ("csa_forward_short_conv", fwd), ("csa_forward_short_conv_f32", fwd),
+                       ("csa_forward_logdomain", fwd),
                        ("csa_std_forward", std), ("csa_std_forward_f32", std),
                        ("csa_forward_symmetric", std), ("csa_forward_symmetric_f32", std),
                        ("csa_logphi2_eval", [p, p, i, p]),
@@ -126,14 +127,17 @@ def _check_tensor(t, name, dtype, shape, device):
 
 
 def forward(q, k, v, k0=None, v0=None, *, mode: int = 0, scale=None, out=None, lse=None,
-            stream=None, want_lse: bool = True, short_conv: bool = False):
+            stream=None, want_lse: bool = True, short_conv: bool = False,
+            log_domain: bool = False):
     """Causal continuous softmax attention.  Returns (o, lse).
 
     q, k, v: CUDA tensors [B, H, T, d], all bf16 (tensor-core kernel for
     d in {64, 128}) or all fp32 (CUDA-core kernel).  k0, v0: [H, d], read
     in mode GIVEN (2).  mode: 0 zero sink, 1 copy of the first token,
     2 given.  scale defaults to 1/sqrt(d).  short_conv=True runs the
-    first-order (eq. (13)) reading instead (csa_forward_short_conv)."""
+    first-order (eq. (13)) reading instead (csa_forward_short_conv);
+    log_domain=True forms the same weights as z = a + b in the log domain
+    (csa_forward_logdomain; bf16 only: the fp32 kernel already does)."""
     import torch
 
     B, H, T, d = q.shape
@@ -160,7 +164,12 @@ def forward(q, k, v, k0=None, v0=None, *, mode: int = 0, scale=None, out=None, l
     lib = load()
     if dtype not in (torch.bfloat16, torch.float32):
         raise ValueError(f"unsupported dtype {dtype}")
-    where = ("csa_forward_short_conv" if short_conv else "csa_forward") + (
+    if short_conv and log_domain:
+        raise ValueError("short_conv and log_domain are separate forms")
+    if log_domain and dtype != torch.bfloat16:
+        raise ValueError("log_domain is a bf16 form (csa_forward_f32 forms b in the log domain)")
+    where = ("csa_forward_short_conv" if short_conv else
+             "csa_forward_logdomain" if log_domain else "csa_forward") + (
         "" if dtype == torch.bfloat16 else "_f32")
     fn = getattr(lib, where)
     _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(k0), _ptr(v0), _ptr(out), _ptr(lse),

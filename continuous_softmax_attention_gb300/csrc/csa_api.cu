@@ -68,8 +68,9 @@ int forward_bf16(const void *q, const void *k, const void *v, const void *k0, co
             return csa_tc_forward(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode, form, s);
         return csa_tc_std_forward(q, k, v, out, lse, B, H, T, d, scale, s);
     }
+    // the CUDA-core kernel forms b in the log domain in its exact form
     return from_cuda(csa_simt_forward_bf16(q, k, v, k0, v0, out, lse, B, H, T, d, scale, mode,
-                                           form, s));
+                                           form == kFormLogDomain ? kFormExact : form, s));
 }
 
 int forward_f32(const float *q, const float *k, const float *v, const float *k0, const float *v0,
@@ -336,6 +337,13 @@ int csa_forward_short_conv(const void *q, const void *k, const void *v, const vo
                            const void *v0, void *out, float *lse, int B, int H, int T, int d,
                            float scale, int k0_mode, csa_stream_t stream) {
     return forward_bf16(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, kFormShortConv,
+                        stream);
+}
+
+int csa_forward_logdomain(const void *q, const void *k, const void *v, const void *k0,
+                          const void *v0, void *out, float *lse, int B, int H, int T, int d,
+                          float scale, int k0_mode, csa_stream_t stream) {
+    return forward_bf16(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, kFormLogDomain,
                         stream);
 }
 

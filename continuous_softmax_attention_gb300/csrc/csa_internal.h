@@ -5,9 +5,10 @@
 #include <cuda_runtime.h>
 
 // Forms of the forward pass: eq. (10)/(11), the short-conv reading of
-// eq. (13) (b replaced by its first-order term), eq. (12), and eq. (2) over
-// the symmetric interval [1/2, t + 1/2] (constant end half-cells, no sink).
-enum { kFormExact = 0, kFormShortConv = 1, kFormStd = 2, kFormSymmetric = 3 };
+// eq. (13) (b replaced by its first-order term), eq. (12), eq. (2) over
+// the symmetric interval [1/2, t + 1/2] (constant end half-cells, no sink),
+// and eq. (10)/(11) evaluated in the log domain (z = a + b, then e^z).
+enum { kFormExact = 0, kFormShortConv = 1, kFormStd = 2, kFormSymmetric = 3, kFormLogDomain = 4 };
 
 // CUDA-core kernels (csa_simt.cu).
 cudaError_t csa_simt_forward_f32(const float *q, const float *k, const float *v, const float *k0,
@@ -20,7 +21,7 @@ cudaError_t csa_simt_logphi2_eval(const float *x, float *y, int n, cudaStream_t 
 
 // Tensor-core kernels, d in {64, 128}, bf16.  Return a CSA_* status code
 // (CSA_OK on success).  Continuous attention, form kFormExact,
-// kFormShortConv or kFormSymmetric (csa_tc.cu):
+// kFormShortConv, kFormSymmetric or kFormLogDomain (csa_tc.cu):
 int csa_tc_forward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
                    void *out, float *lse, int B, int H, int T, int d, float scale, int mode,
                    int form, cudaStream_t stream);

@@ -93,6 +93,9 @@ constexpr int kThreads = 32 * 10;
 constexpr float kLseShift = 0.7330258411633287f;
 // |X| below this (log2 units) takes the small-step coefficients.
 constexpr float kTau = 0.0625f;
+// the kernel's forms (template argument): interval weights, the short-conv
+// reading, and the log-domain evaluation of the interval weights
+constexpr int kTcExact = 0, kTcShort = 1, kTcLog = 2;
 // A half-cell p/2 of the symmetric interval, times the common (ln 2)^2.
 constexpr float kHalfCell = 0.5f * kLn2 * kLn2;
 // A chunk whose weights sum past this raises its half's running max.
@@ -542,6 +545,88 @@ __device__ __forceinline__ void short_chunk(const float (&s)[NCK + 1], const Row
     }
 }
 
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// log2 phi2(x) and log2 phi2(-x) of one logit step x (natural units), from
+// MUFU exp2/log2: |x| <= 1 from the power series of the integral definition
+// (even and odd parts shared by both signs, seven terms: below 3e-6
+// relative); |x| > 1 from e^{|x|} - 1 - |x| = e^{|x|} (1 - (1 + |x|) e^{-|x|})
+// and e^{-|x|} - 1 + |x|, both free of cancellation there.
+__device__ __forceinline__ void lg2_phi2_pm(float x, float &lp, float &lm) {
+    const float ax = fabsf(x), x2 = x * x;
+    const float ev = fmaf(x2, fmaf(x2, fmaf(x2, 1.0f / 40320.0f, 1.0f / 720.0f), 1.0f / 24.0f), 0.5f);
+    const float od = x * fmaf(x2, fmaf(x2, 1.0f / 5040.0f, 1.0f / 120.0f), 1.0f / 6.0f);
+    const float sp = lg2_approx(ev + od), sm = lg2_approx(ev - od);
+    const float e = ex2_approx(-ax * kLog2e), l2ax = lg2_approx(ax);
+    const float bpos = fmaf(ax, kLog2e, lg2_approx(fmaf(-(1.0f + ax), e, 1.0f))) - 2.0f * l2ax;
+    const float bneg = lg2_approx(e - 1.0f + ax) - 2.0f * l2ax;
+    const bool small = ax <= 1.0f, pos = x > 0.0f;
+    lp = small ? sp : (pos ? bpos : bneg);
+    lm = small ? sm : (pos ? bneg : bpos);
+}
+
+// The log-domain evaluation of the same weights, eq. (10)/(11) as written:
+// a key's weight is 2^z, z = u + log2(phi2(a_{c-1} - a_c) + phi2(a_{c+1} - a_c))
+// (u in log2 units relative to the running max), the two log2 phi2 added by
+// a log-domain sum; one-sided at the sink (right neighbour only) and at each
+// row's last key (left neighbour only).  These are cont_chunk's weights
+// without the common (ln 2)^2 factor, formed with about nine MUFU
+// operations per key where cont_chunk takes two.  Arguments as short_chunk.
+template <int NCK, bool MASKED, bool EDGE_L, bool EDGE_R>
+__device__ __forceinline__ void log_chunk(const float (&s)[NCK + 1], const RowState &st, float nm,
+                                          int cb, int c_last, bool halo_l, bool sink, bool halo_r,
+                                          float &ul, uint32_t (&pk)[NCK / 2], float2 &csum,
+                                          float &w1) {
+    float u[NCK + 2];  // u[i + 1] is column cb + i
+    u[0] = ul;
+#pragma unroll
+    for (int i = 0; i <= NCK; ++i) {
+        float sv = s[i];
+        if (EDGE_L && i == 1) {
+            const float alt = st.mode == CSA_K0_GIVEN ? st.s_sink : s[2];
+            sv = sink && st.mode != CSA_K0_ZERO ? alt : sv;
+        }
+        u[i + 1] = fmaf(sv, st.k2, nm);
+    }
+    ul = u[NCK];
+    // interval q joins columns cb + q - 1 and cb + q
+    float lp[NCK + 1], lm[NCK + 1];
+#pragma unroll
+    for (int q = 0; q <= NCK; ++q) lg2_phi2_pm((u[q + 1] - u[q]) * kLn2, lp[q], lm[q]);
+    float W[NCK];
+#pragma unroll
+    for (int i = 0; i < NCK; ++i) {
+        const int c = cb + i;
+        const float l = lm[i], r = lp[i + 1];  // phi2(a_{c-1} - a_c), phi2(a_{c+1} - a_c)
+        const float hi = fmaxf(l, r), lo = fminf(l, r);
+        float b = hi + lg2_approx(1.0f + ex2_approx(lo - hi));
+        if (EDGE_L && i == 1) b = sink ? r : b;
+        if (MASKED) b = c == c_last ? l : b;
+        float w = ex2_approx(u[i + 1] + b);
+        if (MASKED) w = c <= c_last ? w : 0.0f;
+        W[i] = w;
+    }
+    if (EDGE_L) W[0] = halo_l ? 0.0f : W[0];
+    if (EDGE_R) W[NCK - 1] = halo_r ? 0.0f : W[NCK - 1];
+    w1 = W[1];
+    if (EDGE_L) {
+        const bool copy = sink && st.mode == CSA_K0_COPY_FIRST;
+        const bool given = sink && st.mode == CSA_K0_GIVEN;
+        W[2] = copy ? W[2] + W[1] : W[2];
+        W[1] = copy || given ? 0.0f : W[1];
+    }
+    float2 t = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < NCK; i += 2) t = __fadd2_rn(t, make_float2(W[i], W[i + 1]));
+    csum = t;
+#pragma unroll
+    for (int m = 0; m < NCK / 2; ++m) pk[m] = pack_bf16x2(W[2 * m], W[2 * m + 1]);
+}
+
 // Max of the valid scaled logits a*log2(e) of one half-row in the query
 // tile's first key tile: the half's columns and the neighbour column its
 // intervals reach (columns c0..c0+h0, c0 = h (h0 - 1)), read in one batch
@@ -666,11 +751,12 @@ __device__ __noinline__ float2 raise_running_max(uint32_t tS, uint32_t tO, int c
 // half's keys (columns kb..kb+h0-1, kb = h h0), held as bf16 in registers,
 // checked, then written as P_h over the half's own S columns (64 keys,
 // zero beyond the half).  Returns false if a wait expired.
-template <int D, bool SHORT, bool SYM, bool MASKED>
+template <int D, int FORM, bool SYM, bool MASKED>
 __device__ __forceinline__ bool half_tile(uint32_t tS, uint32_t tO, RowState &st, int h,
                                           int c_last, bool first, bool rescale_o, uint32_t odone,
                                           uint32_t parity, volatile int *abort_flag) {
     using C = TcCfg<D>;
+    constexpr bool SHORT = FORM == kTcShort, LOGD = FORM == kTcLog;
     constexpr int NK = C::kNK, H0 = C::kH0, NL = H0 - 48;
     const int kb = h * H0;
     // two chunks: 32 keys, then the remaining NB2 (24 or 32)
@@ -708,7 +794,7 @@ __device__ __forceinline__ bool half_tile(uint32_t tS, uint32_t tO, RowState &st
         // the share key kb receives from interval (kb-1, kb) (exact), or the
         // u of column kb-1 (short); for half 0, column 0 is a halo: unused
         float carry;
-        if (SHORT) {
+        if (SHORT || LOGD) {
             carry = fmaf(lg[0], st.k2, nm);
         } else {
             const float u0 = fmaf(lg[0], st.k2, nm), u1 = fmaf(lg[1], st.k2, nm);
@@ -729,6 +815,9 @@ __device__ __forceinline__ bool half_tile(uint32_t tS, uint32_t tO, RowState &st
             if (SHORT)
                 short_chunk<NC, MASKED, EL, ER>(s, st, nm, kb + off, c_last, h == 0, first && h == 0,
                                                 h == 1, carry, pk, cs, w1c);
+            else if (LOGD)
+                log_chunk<NC, MASKED, EL, ER>(s, st, nm, kb + off, c_last, h == 0, first && h == 0,
+                                              h == 1, carry, pk, cs, w1c);
             else
                 cont_chunk<NC, MASKED, SYM, EL, ER>(s, st, nm, kb + off, c_last, h == 0,
                                                    first && h == 0, h == 1, carry, pk, cs, w1c);
@@ -795,7 +884,7 @@ __device__ __forceinline__ bool half_tile(uint32_t tS, uint32_t tO, RowState &st
     return true;
 }
 
-template <int D, bool SHORT, bool SYM>
+template <int D, int FORM, bool SYM>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_forward_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -1081,9 +1170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool masked = KS * (j + 1) > row0 + 1;
                 if (j == 0) st.m = first_tile_max<C::kH0, SYM>(tS, st, h * (C::kH0 - 1), c_last);
                 const uint32_t odone = BAR(C::kBarODone), par = (g - 1) & 1;
-                ok = masked ? half_tile<D, SHORT, SYM, true>(tS, tO, st, h, c_last, j == 0, j > 0,
+                ok = masked ? half_tile<D, FORM, SYM, true>(tS, tO, st, h, c_last, j == 0, j > 0,
                                                              odone, par, abort_flag)
-                            : half_tile<D, SHORT, SYM, false>(tS, tO, st, h, c_last, j == 0, j > 0,
+                            : half_tile<D, FORM, SYM, false>(tS, tO, st, h, c_last, j == 0, j > 0,
                                                               odone, par, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
@@ -1175,7 +1264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (store && h == 0 && p.lse)
                 p.lse[(size_t)bh * T + r] =
-                    (mx + log2f(fmaf(a0, l0, a1 * l1))) * kLn2 + (SHORT ? 0.0f : kLseShift);
+                    (mx + log2f(fmaf(a0, l0, a1 * l1))) * kLn2 + (FORM == kTcExact ? kLseShift : 0.0f);
             tc_fence_before();
         }
         // the output stores are complete before the block exits
@@ -1265,7 +1354,7 @@ int launch_with_slot(int dev, cudaStream_t stream, Launch &&launch) {
     return CSA_OK;
 }
 
-template <int D, bool SHORT, bool SYM>
+template <int D, int FORM, bool SYM>
 int launch_tc(const void *q, const void *k, const void *v, const void *k0, const void *v0,
               void *out, float *lse, int B, int H, int T, float scale, int mode,
               cudaStream_t stream) {
@@ -1295,7 +1384,7 @@ int launch_tc(const void *q, const void *k, const void *v, const void *k0, const
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
         return CSA_ERR_CUDA;
     const unsigned grid = (unsigned)(items < sms ? items : sms);  // one CTA per SM
-    auto kern = tc_forward_kernel<D, SHORT, SYM>;
+    auto kern = tc_forward_kernel<D, FORM, SYM>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return CSA_ERR_CUDA;
@@ -1315,16 +1404,20 @@ int csa_tc_forward(const void *q, const void *k, const void *v, const void *k0, 
     return launch_tc<DD, SC, SY>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode, stream)
     if (d != 64 && d != 128) return CSA_ERR_UNSUPPORTED;
     if (form == kFormShortConv) {
-        if (d == 128) CSA_TC_LAUNCH(128, true, false);
-        CSA_TC_LAUNCH(64, true, false);
+        if (d == 128) CSA_TC_LAUNCH(128, kTcShort, false);
+        CSA_TC_LAUNCH(64, kTcShort, false);
+    }
+    if (form == kFormLogDomain) {
+        if (d == 128) CSA_TC_LAUNCH(128, kTcLog, false);
+        CSA_TC_LAUNCH(64, kTcLog, false);
     }
     if (form == kFormSymmetric) {  // no sink: mode is ignored
         mode = CSA_K0_ZERO;
-        if (d == 128) CSA_TC_LAUNCH(128, false, true);
-        CSA_TC_LAUNCH(64, false, true);
+        if (d == 128) CSA_TC_LAUNCH(128, kTcExact, true);
+        CSA_TC_LAUNCH(64, kTcExact, true);
     }
-    if (d == 128) CSA_TC_LAUNCH(128, false, false);
-    CSA_TC_LAUNCH(64, false, false);
+    if (d == 128) CSA_TC_LAUNCH(128, kTcExact, false);
+    CSA_TC_LAUNCH(64, kTcExact, false);
 #undef CSA_TC_LAUNCH
 }
 

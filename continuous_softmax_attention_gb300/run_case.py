@@ -33,6 +33,8 @@ def main():
     ap.add_argument("--backward", action="store_true")
     ap.add_argument("--short-conv", action="store_true",
                     help="the first-order (eq. (13)) form instead of the exact one")
+    ap.add_argument("--log-domain", action="store_true",
+                    help="the exact form's weights formed in the log domain")
     a = ap.parse_args()
     if a.decode:
         return run_decode(a)
@@ -43,7 +45,7 @@ def main():
     scale = 1.0 / math.sqrt(a.d)
     for _ in range(a.iters):
         o, lse = csa.forward(g["q"], g["k"], g["v"], g["k0"], g["v0"], mode=a.mode, scale=scale,
-                             short_conv=a.short_conv)
+                             short_conv=a.short_conv, log_domain=a.log_domain)
         if not a.no_std:
             csa.std_forward(g["q"], g["k"], g["v"], scale=scale)
     torch.cuda.synchronize()

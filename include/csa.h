@@ -181,6 +181,25 @@ int csa_forward_short_conv(const void *q, const void *k, const void *v, const vo
                            const void *v0, void *out, float *lse, int B, int H, int T, int d,
                            float scale, int k0_mode, csa_stream_t stream);
 
+/*
+ * csa_forward_logdomain - csa_forward with the weights formed as eq. (10)
+ *   and (11) of "Continuous Softmax Attention" ("Assembly and
+ *   Simplification") write them: per key, z = a + b with
+ *   b = log(phi2(a_{i-1} - a_i) + phi2(a_{i+1} - a_i)) (one-sided at the
+ *   sink and at the row's own key) from log phi2 of each logit step, added
+ *   in the log domain, and then e^{z - m}.  The same result as csa_forward
+ *   (which forms each key's weight from the two interval shares of eq. (9)
+ *   with one exponential and one reciprocal) within the bf16 rounding of
+ *   the weights; it takes about nine special-function operations per
+ *   (query, key) pair where csa_forward takes two, and is kept as the
+ *   reference evaluation of that step.  Same arguments, layout, alignment,
+ *   d rules (d other than 64 and 128 runs the CUDA-core kernel, which
+ *   forms b this way too), sink modes and errors as csa_forward.
+ */
+int csa_forward_logdomain(const void *q, const void *k, const void *v, const void *k0,
+                          const void *v0, void *out, float *lse, int B, int H, int T, int d,
+                          float scale, int k0_mode, csa_stream_t stream);
+
 /* csa_forward_short_conv_f32 - the same in fp32 on CUDA cores, 1 <= d <= 256. */
 int csa_forward_short_conv_f32(const float *q, const float *k, const float *v, const float *k0,
                                const float *v0, float *out, float *lse, int B, int H, int T,
