@@ -61,3 +61,23 @@ def test_short_conv_headline_sampled():
     go = o.reshape(-1, d)[torch.as_tensor(flat)]
     gl = lse.reshape(-1)[torch.as_tensor(flat)]
     assert_close(go, gl, ro, rl, "bf16", "headline rows")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_short_conv_running_max_raised(d, mode):
+    """Keys far into the sequence whose logits exceed every earlier one by
+    hundreds (log2 units): the running max is raised (at d = 128 by both
+    column halves together, as they share one accumulator) and what was
+    written rescaled.  The oracle is exact for any logits."""
+    T = 700
+    x = make_inputs(1, 2, T, d, "bf16", seed=230 + d)
+    k = x["k"].float()
+    for pos, f in ((300, 25.0), (301, 25.0), (450, 60.0), (640, 90.0)):
+        k[:, :, pos] = k[:, :, pos] * f
+    x["k"] = k.to(torch.bfloat16)
+    scale = 1.0 / d ** 0.5
+    o, lse = run(x, scale, mode)
+    ro, rl = oracle.forward_short_conv(x["q"], x["k"], x["v"], x["k0"], x["v0"], scale=scale,
+                                       mode=mode)
+    assert_close(o, lse, ro, rl, "bf16", f"short conv, max raised d={d} mode={mode}")
