@@ -1130,6 +1130,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok || w.n == 0) break;
             const int bh = w.bh, row0 = w.row0, n = w.n;
             const int r = row0 + irow;
+            // this item's first products overwrite O_0 and O_1, which every
+            // softmax thread read in the previous item's epilogue (the second
+            // phase of that item on the exchange barrier)
+            if (c > 0) {
+                ok = __all_sync(0xffffffffu, wait_c(xbar, 1, abort_flag));
+                if (!ok) break;
+            }
             RowState st;
             st.k2 = p.k2;
             st.m = -INFINITY;
@@ -1187,7 +1194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mine[2] = st.w_sink;
             mbar_arrive(xbar);
             // sleeping: the MMA thread is issuing this item's last PV meanwhile
-            ok = __all_sync(0xffffffffu, wait_s(xbar, c & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, wait_s(xbar, 0, abort_flag));
             if (!ok) break;
             const float *oth = xfin + ((h ^ 1) * 128 + irow) * 4;
             const float m0 = h ? oth[0] : st.m, m1 = h ? st.m : oth[0];
@@ -1252,6 +1259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                 }
             }
+            // this thread's reads of O are done: the item's second phase on
+            // the exchange barrier
+            tc_fence_before();
+            mbar_arrive(xbar);
             if (C::kTmaOut) {
                 // one TMA store of the warp's 32 rows x 64 columns (rows past T
                 // are not written; a box wholly past T is not issued)
