@@ -24,6 +24,7 @@ from ._lib import (  # noqa: F401
     forward_symmetric,
     logphi2_eval,
     segment_weights_eval,
+    selftest_forward_delay,
     selftest_wait_timeout,
     shard_rows,
     status_string,
@@ -37,5 +38,6 @@ __all__ = [
     "backward_workspace_bytes", "decode", "decode_noalloc", "decode_workspace_bytes",
     "decode_range", "decode_range_workspace_bytes", "decode_merge_ranges", "shard_rows",
     "logphi2_eval",
-    "segment_weights_eval", "device_status", "selftest_wait_timeout", "status_string",
+    "segment_weights_eval", "device_status", "selftest_forward_delay", "selftest_wait_timeout",
+    "status_string",
 ]

@@ -57,6 +57,8 @@ def load():
                        ("csa_segment_weights_eval", [p, p, p, p, i, p]),
                        ("csa_device_status", []),
                        ("csa_selftest_wait_timeout", [u, p]),
+                       ("csa_selftest_forward_delay", [p, p, p, p, p, p, p, i, i, i, i, f, i, u,
+                                                       i, p]),
                        ("csa_abi_version", []),
                        ("csa_decode", [p, p, p, p, p, p, p, p, p, ctypes.c_longlong, i, i, i, i,
                                        f, i, p]),
@@ -572,6 +574,36 @@ def segment_weights_eval(u0, u1, stream=None):
 def device_status() -> int:
     """Reads and clears the library's device status word (synchronises)."""
     return int(load().csa_device_status())
+
+
+def selftest_forward_delay(q, k, v, k0=None, v0=None, *, mode: int = 0, scale=None,
+                           delay_ns: int = 20000, delay_half: int = 1, stream=None):
+    """csa_forward's exact form (bf16, d in {64, 128}) with a delay planted
+    before each epilogue's reads of the accumulators, for one column half
+    (csa_selftest_forward_delay).  Returns (o, lse), which must equal
+    forward()'s bit for bit."""
+    import torch
+
+    B, H, T, d = q.shape
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(t, name, torch.bfloat16, (B, H, T, d), dev)
+    if mode == 2:
+        if k0 is None or v0 is None:
+            raise ValueError("mode 2 (given sink) needs k0 and v0")
+        _check_tensor(k0, "k0", torch.bfloat16, (H, d), dev)
+        _check_tensor(v0, "v0", torch.bfloat16, (H, d), dev)
+    else:
+        k0 = v0 = None
+    if scale is None:
+        scale = 1.0 / d ** 0.5
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    _check(load().csa_selftest_forward_delay(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(k0), _ptr(v0), _ptr(out), _ptr(lse), B, H, T, d,
+        float(scale), int(mode), int(delay_ns), int(delay_half), _stream_handle(stream)),
+        "csa_selftest_forward_delay")
+    return out, lse
 
 
 def selftest_wait_timeout(timeout_us: int, stream=None):

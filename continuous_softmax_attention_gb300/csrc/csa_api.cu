@@ -422,6 +422,24 @@ int csa_selftest_wait_timeout(unsigned timeout_us, csa_stream_t stream) {
     return from_cuda(csa_tc_selftest_wait_timeout(timeout_us, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int csa_selftest_forward_delay(const void *q, const void *k, const void *v, const void *k0,
+                               const void *v0, void *out, float *lse, int B, int H, int T, int d,
+                               float scale, int k0_mode, unsigned delay_ns, int delay_half,
+                               csa_stream_t stream) {
+    if (delay_ns > 1000000u || (delay_half != 0 && delay_half != 1)) return CSA_ERR_INVALID_ARG;
+    bool empty;
+    int rc = check_common(q, k, v, k0, v0, out, B, H, T, d, scale, k0_mode, true, &empty);
+    if (rc != CSA_OK || empty) return rc;
+    if (d != 64 && d != 128) return CSA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+        (lse && !aligned(lse, 4)))
+        return CSA_ERR_ALIGNMENT;
+    if (k0_mode == CSA_K0_GIVEN && (!aligned(k0, 2) || !aligned(v0, 2))) return CSA_ERR_ALIGNMENT;
+    if ((rc = device_ok()) != CSA_OK) return rc;
+    return csa_tc_forward_delayed(q, k, v, k0, v0, out, lse, B, H, T, d, scale, k0_mode, delay_ns,
+                                  delay_half, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int csa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, const void *k0,
                        const void *v0, const int *seqlens, void *out, float *lse, int B, int H,
                        int T, int d, float scale, int k0_mode, csa_stream_t stream) {

@@ -25,6 +25,12 @@ cudaError_t csa_simt_logphi2_eval(const float *x, float *y, int n, cudaStream_t 
 int csa_tc_forward(const void *q, const void *k, const void *v, const void *k0, const void *v0,
                    void *out, float *lse, int B, int H, int T, int d, float scale, int mode,
                    int form, cudaStream_t stream);
+// The exact form with a planted delay in the epilogue (test hook): the
+// softmax threads of column half delay_half sleep delay_ns before reading O.
+int csa_tc_forward_delayed(const void *q, const void *k, const void *v, const void *k0,
+                           const void *v0, void *out, float *lse, int B, int H, int T, int d,
+                           float scale, int mode, unsigned delay_ns, int delay_half,
+                           cudaStream_t stream);
 // Standard causal attention, eq. (12) (csa_tc_std.cu):
 int csa_tc_std_forward(const void *q, const void *k, const void *v, void *out, float *lse, int B,
                        int H, int T, int d, float scale, cudaStream_t stream);

@@ -170,6 +170,10 @@ struct TcParams {
     float *lse;
     int num_items;  // query tiles: num_qtiles * B * H
     int slot;       // this launch's scheduling counters
+    // test hook: the softmax threads of column half delay_half sleep
+    // delay_ns before reading O in each epilogue (0: none)
+    unsigned delay_ns;
+    int delay_half;
 };
 
 // A work item is one query tile of one (b, h).  Heads go in groups whose K/V
@@ -1206,6 +1210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // first PV waits for this thread's PFull arrival, after the reads
             ok = __all_sync(0xffffffffu, wait_s(BAR(C::kBarODone), (g - 1) & 1, abort_flag));
             if (!ok) break;
+            if (p.delay_ns != 0u && h == p.delay_half) __nanosleep(p.delay_ns);
             tc_fence_after();
             const uint32_t tO0 = tmem + lane_off + C::col_o(0), tO1 = tmem + lane_off + C::col_o(1);
             // o is divided by the sum of exactly the bf16 weights that fed the
@@ -1368,7 +1373,7 @@ int launch_with_slot(int dev, cudaStream_t stream, Launch &&launch) {
 template <int D, int FORM, bool SYM>
 int launch_tc(const void *q, const void *k, const void *v, const void *k0, const void *v0,
               void *out, float *lse, int B, int H, int T, float scale, int mode,
-              cudaStream_t stream) {
+              cudaStream_t stream, unsigned delay_ns = 0u, int delay_half = 0) {
     using C = TcCfg<D>;
     const int BH = B * H;
     CUtensorMap mq, mk, mv, mo;
@@ -1387,6 +1392,8 @@ int launch_tc(const void *q, const void *k, const void *v, const void *k0, const
     prm.v0 = static_cast<const __nv_bfloat16 *>(v0);
     prm.out = static_cast<__nv_bfloat16 *>(out);
     prm.lse = lse;
+    prm.delay_ns = delay_ns;
+    prm.delay_half = delay_half;
     const long long items = (long long)prm.num_qtiles * BH;
     if (items > 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
     prm.num_items = (int)items;
@@ -1430,6 +1437,19 @@ int csa_tc_forward(const void *q, const void *k, const void *v, const void *k0, 
     if (d == 128) CSA_TC_LAUNCH(128, kTcExact, false);
     CSA_TC_LAUNCH(64, kTcExact, false);
 #undef CSA_TC_LAUNCH
+}
+
+int csa_tc_forward_delayed(const void *q, const void *k, const void *v, const void *k0,
+                           const void *v0, void *out, float *lse, int B, int H, int T, int d,
+                           float scale, int mode, unsigned delay_ns, int delay_half,
+                           cudaStream_t stream) {
+    if (d == 128)
+        return launch_tc<128, kTcExact, false>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode,
+                                               stream, delay_ns, delay_half);
+    if (d == 64)
+        return launch_tc<64, kTcExact, false>(q, k, v, k0, v0, out, lse, B, H, T, scale, mode,
+                                              stream, delay_ns, delay_half);
+    return CSA_ERR_UNSUPPORTED;
 }
 
 cudaError_t csa_tc_segment_weights_eval(const float *u0, const float *u1, float *right,

@@ -455,6 +455,25 @@ int csa_device_status(void);
  */
 int csa_selftest_wait_timeout(unsigned timeout_us, csa_stream_t stream);
 
+/*
+ * csa_selftest_forward_delay - csa_forward's exact form (the tensor-core
+ *   kernel, bf16, d in {64, 128}; arguments, layout, ownership and checks as
+ *   csa_forward) with a delay planted in every epilogue: the softmax threads
+ *   of column half delay_half (0 or 1) sleep delay_ns nanoseconds (at most
+ *   10^6) after the item's last PV product is done and before they read the
+ *   two accumulators O_0 and O_1.  Meanwhile the other half's threads run
+ *   ahead into the CTA's next query tile, whose first PV product overwrites
+ *   O_0 and O_1 ("Assembly and Simplification", eq. (10): the numerator and
+ *   denominator sums per query row).  The kernel orders that product after
+ *   every thread's reads, so the output and lse must equal csa_forward's bit
+ *   for bit whatever the delay.  CSA_ERR_INVALID_ARG for a delay or half out
+ *   of range.  A test hook: it only slows the kernel down.
+ */
+int csa_selftest_forward_delay(const void *q, const void *k, const void *v, const void *k0,
+                               const void *v0, void *out, float *lse, int B, int H, int T, int d,
+                               float scale, int k0_mode, unsigned delay_ns, int delay_half,
+                               csa_stream_t stream);
+
 /* Human-readable text for a status code (never NULL, static storage). */
 const char *csa_status_string(int status);
 

@@ -75,6 +75,14 @@ def test_std_and_f32_validation(lib):
     assert lib.csa_forward_f32(ctypes.c_void_p(4097), FAKE, FAKE, NULL, NULL, FAKE, NULL, 1, 1, 4, 16, 0.1, 0, None) == L.CSA_ERR_ALIGNMENT
     assert lib.csa_selftest_wait_timeout(0, None) == L.CSA_ERR_INVALID_ARG
     assert lib.csa_selftest_wait_timeout(2000000, None) == L.CSA_ERR_INVALID_ARG
+    # the planted-delay forward: delay above 10^6 ns or a half other than 0, 1
+    dly = lambda **kw: lib.csa_selftest_forward_delay(
+        FAKE, FAKE, FAKE, NULL, NULL, FAKE, NULL, 1, 1, 4, kw.get("d", 64), 0.1, 0,
+        kw.get("ns", 1000), kw.get("half", 0), None)
+    assert dly(ns=1000001) == L.CSA_ERR_INVALID_ARG
+    assert dly(half=2) == L.CSA_ERR_INVALID_ARG
+    assert dly(half=-1) == L.CSA_ERR_INVALID_ARG
+    assert dly(d=96) == L.CSA_ERR_UNSUPPORTED
 
 
 def test_no_device_is_reported(lib):
