@@ -112,6 +112,18 @@ def test_stress_workload(scale, mode):
     assert_close(o, lse, ro, rl, "bf16", f"stress scale={scale} mode={mode}")
 
 
+@pytest.mark.parametrize("scale", [0.125, 1.0, 4.0])
+@pytest.mark.parametrize("mode", MODES)
+def test_stress_scales_d128(scale, mode):
+    """The stress workload's scales at d = 128 (112-key tiles, several
+    running-max raises per row at scale 4), B=2, H=4, T=512, every sink
+    mode, full comparison."""
+    x = make_inputs(2, 4, 512, 128, "bf16", seed=2)
+    o, lse = run_csa(x, mode, scale)
+    ro, rl = oracle_csa(x, mode, scale)
+    assert_close(o, lse, ro, rl, "bf16", f"d=128 stress scale={scale} mode={mode}")
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_tc_matches_cuda_core_log_domain_path(d):
     """The tensor-core kernel (interval weights R, L) against the CUDA-core
