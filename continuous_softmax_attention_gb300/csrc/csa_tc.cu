@@ -130,8 +130,14 @@ struct TcCfg {
     // other, so each half's arrivals alternate between two barriers (one
     // phase per two tiles) and none completes twice before it is consumed
     static constexpr int kBarPFull = kBarSFull + 2;
+    // [2]: PV pair k completes a phase of barrier k % 2.  A wait by parity
+    // is unambiguous only while the barrier's previous phase is complete;
+    // with two barriers that phase is PV pair k-2, which every wait below
+    // follows (the S wait of tile k covers every product issued before
+    // S(k), PV pair k-2 among them).  One barrier would need PV pair k-1's
+    // previous phase, k-2, at the epilogue, where nothing waited for it.
     static constexpr int kBarODone = kBarPFull + 4;
-    static constexpr int kBarDrain = kBarODone + 1;
+    static constexpr int kBarDrain = kBarODone + 2;
     static constexpr int kBarX = kBarDrain + 1;       // half-to-half exchange (epilogue)
     static constexpr int kBarQEmpty = kBarX + 1;      // an item's last S is done
     static constexpr int kBarQRead = kBarQEmpty + 1;  // its sink logits are read from Q
@@ -651,6 +657,8 @@ __device__ __forceinline__ float first_tile_max(uint32_t tS, const RowState &st,
     tmem_ld32(tS + c0, a);
     if constexpr (H0 == 64) {
         tmem_ld32(tS + c0 + 32, b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e8[i] = 0u;  // unused at this width
     } else {
         tmem_ld16(tS + c0 + 32, b);
         tmem_ld8(tS + c0 + 48, e8);
@@ -925,7 +933,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(BAR(C::kBarSFull + 0), 1);
         mbar_init(BAR(C::kBarSFull + 1), 1);
         for (int i = 0; i < 4; ++i) mbar_init(BAR(C::kBarPFull + i), 128);
-        mbar_init(BAR(C::kBarODone), 1);
+        mbar_init(BAR(C::kBarODone + 0), 1);
+        mbar_init(BAR(C::kBarODone + 1), 1);
         mbar_init(BAR(C::kBarDrain), 1);
         mbar_init(BAR(C::kBarX), 256);
         mbar_init(BAR(C::kBarQEmpty), 1);
@@ -1099,7 +1108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   (p_j > 0 || kk > 0) ? 1u : 0u);
                 }
                 if (!ok) break;
-                tc_commit(BAR(C::kBarODone));
+                tc_commit(BAR(C::kBarODone + (gp & 1)));
                 tc_commit(BAR(C::kBarVEmpty + gp % NSV));
                 ++gp;
                 ++p_j;
@@ -1180,7 +1189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int c_last = r + 2 - KS * j;
                 const bool masked = KS * (j + 1) > row0 + 1;
                 if (j == 0) st.m = first_tile_max<C::kH0, SYM>(tS, st, h * (C::kH0 - 1), c_last);
-                const uint32_t odone = BAR(C::kBarODone), par = (g - 1) & 1;
+                // PV pair g-1, for a rescale of O_h
+                const uint32_t odone = BAR(C::kBarODone + ((g - 1) & 1)), par = ((g - 1) >> 1) & 1;
                 ok = masked ? half_tile<D, FORM, SYM, true>(tS, tO, st, h, c_last, j == 0, j > 0,
                                                              odone, par, abort_flag)
                             : half_tile<D, FORM, SYM, false>(tS, tO, st, h, c_last, j == 0, j > 0,
@@ -1206,9 +1216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float w_sink = h ? oth[2] : st.w_sink;  // in half 0's scale
             const float mx = fmaxf(m0, m1);
             const float a0 = ex2_approx(m0 - mx), a1 = ex2_approx(m1 - mx);
-            // O holds this item's last PV once it is done; the next item's
-            // first PV waits for this thread's PFull arrival, after the reads
-            ok = __all_sync(0xffffffffu, wait_s(BAR(C::kBarODone), (g - 1) & 1, abort_flag));
+            // O holds this item's last PV pair, g-1, once it is done (the
+            // next item's first PV waits for every softmax thread's reads of
+            // O: the exchange barrier's second phase below)
+            ok = __all_sync(0xffffffffu,
+                            wait_s(BAR(C::kBarODone + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag));
             if (!ok) break;
             if (p.delay_ns != 0u && h == p.delay_half) __nanosleep(p.delay_ns);
             tc_fence_after();
@@ -1222,7 +1234,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld_regs<1>(rs[1]);
             const float den = fmaf(a0, __uint_as_float(rs[0][0]) + w_sink, a1 * __uint_as_float(rs[1][0]));
             const float inv_l = 1.0f / den;
-            const float c0 = a0 * inv_l, c1 = a1 * inv_l;
             const bool store = r < T;
             __nv_bfloat16 *orow =
                 p.out + ((size_t)bh * T + (size_t)(store ? r : 0)) * D + h * (D / 2);
